@@ -1,0 +1,204 @@
+/*
+ * fd_api.h -- C ABI of libfd: paged, GQA-shared, split-KV decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one query token per sequence against its cached keys and
+ * values) is the decode step described on these pages:
+ *   [P1] "FlashDecoding 与 FlashInfer 深度解析" (tbr8.org), §2.1: split the KV
+ *        sequence into contiguous chunks, compute per chunk the scores
+ *        q k^T / sqrt(d), a local softmax, the weighted sum of V and the local
+ *        max and sum, then merge the chunks exactly.
+ *   [P2] lpnh.cn/news/1601758, "FlashDecoding 核心原理": stage one writes the
+ *        partial state (unnormalised O_i, max m_i, denominator d_i); stage two
+ *        merges with m = max m_i, alpha_i = exp(m_i - m), d = sum alpha_i d_i,
+ *        O = sum alpha_i O_i / d; "进阶突破": a cost model picks the split count
+ *        from batch, heads, length and SM count, and short sequences are not
+ *        split; map and reduce may be fused into one kernel through atomics.
+ *   [P3] "Inference Cookbook" (FlashAttention): §4.2 paged pools
+ *        [num_pages, page_size, Hkv, D] and an int32 block table with -1 in
+ *        unused entries; §3.2-3.3 new K/V are written into the cache and the
+ *        cached lengths are not advanced by the call; §3.5 the softmax LSE per
+ *        (batch, head); §6 split-KV with num_splits (0 = automatic) and its
+ *        heuristic; §7 FP8 (E4M3) KV with fp32 descale factors.
+ *   [P4] "FlashAttention 與 FlashInfer:兩大 GPU 注意力後端": page (block) sizes
+ *        must be multiples of 16.
+ *
+ * Conventions for every entry point:
+ *  - All pointers except seq_lens_host (fd_plan) are DEVICE pointers on the
+ *    current CUDA device.  The library never allocates, frees or copies
+ *    device memory; every buffer belongs to the caller.
+ *  - Calls are asynchronous on the given stream (cudaStream_t passed as a
+ *    void*; NULL = the legacy default stream) and never synchronise.
+ *  - Errors found on the host are returned before anything is launched.
+ *    Errors only the device can see (a block-table entry out of range inside
+ *    a live range, a length beyond the plan's capacity, a wait that ran past
+ *    its time limit) are OR-ed into *status_dev as FD_DEV_* bits when
+ *    status_dev is not NULL; the kernel skips the offending access and never
+ *    traps.  fd_status_from_device() maps a status word to an fd_status.
+ *  - Nothing is thrown across the ABI.
+ */
+#ifndef FD_API_H
+#define FD_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FD_API_VERSION 1
+
+typedef enum {
+    FD_OK = 0,
+    FD_ERR_INVALID_ARG = 1,         /* null pointer, bad size, bad alignment          */
+    FD_ERR_UNSUPPORTED = 2,         /* a valid problem this build does not serve      */
+    FD_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < plan->workspace_bytes        */
+    FD_ERR_BAD_PAGE = 4,            /* device saw a block-table entry out of range    */
+    FD_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed              */
+    FD_ERR_CAPACITY = 6,            /* device saw seq_lens[b] above the plan capacity */
+    FD_ERR_TIMEOUT = 7              /* a device-side wait hit its time limit          */
+} fd_status;
+
+/* Bits of the device status word. */
+#define FD_DEV_BAD_PAGE 0x1
+#define FD_DEV_CAPACITY 0x2
+#define FD_DEV_TIMEOUT  0x4
+
+typedef enum { FD_F16 = 0, FD_BF16 = 1, FD_E4M3 = 2, FD_F32 = 3 } fd_dtype;
+
+/* Shapes and types of one decode problem.
+ *   q            [B, Hq, D]                      q_dtype (FD_F16 or FD_BF16)
+ *   k/v pages    [num_pages, page_size, Hkv, D]  kv_dtype; row-major, D fastest
+ *   block_table  int32 [B, max_blocks_per_seq], entry j of row b is the page
+ *                holding tokens [j*page_size, (j+1)*page_size) of sequence b
+ *   seq_lens     int32 [B]
+ *   out          [B, Hq, D]                      out_dtype (q_dtype or FD_F32)
+ *   lse          fp32 [B, Hq], natural log
+ * Constraints: Hq % Hkv == 0 and Hq / Hkv <= 16 (query heads of one KV head
+ * are the contiguous group hq / (Hq / Hkv) == kvh); D in {64, 128};
+ * page_size % 16 == 0 [P4]; kv_dtype FD_E4M3 requires q_dtype FD_BF16 or
+ * FD_F16, otherwise kv_dtype == q_dtype; 1 <= B <= 8192. */
+typedef struct {
+    int B, Hq, Hkv, D;
+    int page_size;
+    int max_blocks_per_seq;
+    int num_pages;
+    fd_dtype q_dtype, kv_dtype, out_dtype;
+} fd_problem;
+
+typedef struct {
+    int num_splits;     /* 0 = cost model [P2 进阶突破, P3 §6.3]; >0 forces the
+                           number of contiguous chunks of the longest sequence   */
+    int num_sms;        /* 0 = query the device; >0 overrides (planning only)   */
+    int fuse_merge;     /* 1 = the CTA that finishes the last chunk of a (b, kvh)
+                           merges in place (default); 0 = a separate merge kernel */
+    int max_seq_len;    /* 0 = max of seq_lens_host; otherwise the capacity the
+                           plan must cover when it is reused as lengths grow    */
+    int ctas_per_sm;    /* 0 = automatic; persistent CTAs per SM                */
+    int split_margin_pct; /* 0 = default (2): pick the fewest splits whose
+                           estimated time is within this many percent of the
+                           best; 18 reproduces the cookbook's "smallest split
+                           count reaching 85% of the best efficiency" [P3 §6.3] */
+} fd_plan_options;
+
+/* A plan: plain data in host memory, owned by the caller, reusable for any
+ * number of calls while 0 <= seq_lens[b] <= capacity_tokens on the device. */
+typedef struct {
+    fd_problem problem;
+    int num_splits;       /* partial-state slots per (b, hq)                     */
+    int chunk_tokens;     /* tokens per split (a multiple of tile_tokens)        */
+    int tile_tokens;      /* tokens per pipeline stage                           */
+    int capacity_tokens;  /* num_splits * chunk_tokens                           */
+    int grid_ctas;        /* persistent CTAs launched                            */
+    int num_sms;
+    int fuse_merge;
+    int stages;           /* shared-memory pipeline depth                        */
+    int smem_bytes;       /* dynamic shared memory per CTA                       */
+    size_t workspace_bytes;
+    size_t ws_partial_o;  /* byte offsets inside the workspace                   */
+    size_t ws_partial_md;
+    size_t ws_counters;
+    long long work_items_hint; /* items for the host lengths (information)      */
+    int reserved[8];
+} fd_plan_t;
+
+/* Plan a decode call [P1 §2.1 step 1; P2 进阶突破; P3 §6.3, §8.2].
+ *   problem        shapes/types (copied into the plan)
+ *   seq_lens_host  HOST int32 [B]: the lengths the split count is chosen for
+ *   options        may be NULL (all defaults)
+ *   plan           out: filled on FD_OK
+ * The split count follows the pages' rules: no split when the sequences are
+ * short or when B*Hkv already fills the SMs with equal work; otherwise the
+ * smallest split count whose estimated SM efficiency is within a margin of
+ * the best.  The workspace the call needs is plan->workspace_bytes; it must be
+ * zero-filled once after allocation (the kernels leave their counters at zero
+ * when they finish), and again after any call reported an FD_DEV_* error.
+ * Returns FD_ERR_INVALID_ARG / FD_ERR_UNSUPPORTED on bad problems, FD_ERR_CUDA
+ * if the device cannot be queried. */
+fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host,
+                  const fd_plan_options *options, fd_plan_t *plan);
+
+/* One decode step [P1 §2.1; P2 stages one and two; P3 §3.5, §4, §6, §7].
+ *   q, k_pages, v_pages  device, 16-byte aligned, layouts as in fd_problem
+ *   k_scale, v_scale     device fp32 [num_pages, Hkv] for FD_E4M3 (value =
+ *                        e4m3 code * scale); must be NULL otherwise
+ *   block_table, seq_lens device int32; the call attends over tokens
+ *                        [0, seq_lens[b]) of every sequence
+ *   out                  device [B, Hq, D] in problem.out_dtype
+ *   lse                  device fp32 [B, Hq] or NULL
+ *   workspace            device, 256-byte aligned, >= plan->workspace_bytes,
+ *                        zero-filled before its first use; one workspace per
+ *                        call in flight (calls sharing one must not overlap)
+ *   status_dev           device int32 or NULL; FD_DEV_* bits are OR-ed in
+ *   stream               cudaStream_t
+ * A sequence of length 0 gives out = 0 and lse = -inf.  Output rounding is
+ * round-to-nearest-even from fp32. */
+fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pages,
+                          const void *v_pages, const float *k_scale, const float *v_scale,
+                          const int32_t *block_table, const int32_t *seq_lens, void *out,
+                          float *lse, void *workspace, size_t workspace_bytes,
+                          int32_t *status_dev, void *stream);
+
+/* Merge S partial states per (b, hq) into the output [P1 §2.1 step 3 merge;
+ * P2 stage two].
+ *   o_part   device fp32 [B, Hq, S, D]: unnormalised sum_t exp(s_t - m) v_t
+ *   m        device fp32 [B, Hq, S]: max score of the chunk (natural units,
+ *            score = q.k/sqrt(D)); -inf marks an empty chunk
+ *   d        device fp32 [B, Hq, S]: sum_t exp(s_t - m); 0 for an empty chunk
+ *   out      device [B, Hq, D] in out_dtype (FD_F16, FD_BF16 or FD_F32)
+ *   lse      device fp32 [B, Hq] or NULL
+ * All-empty rows give out = 0 and lse = -inf.  1 <= S <= 4096, D <= 256. */
+fd_status fd_merge_states(const float *o_part, const float *m, const float *d, int B, int Hq,
+                          int S, int D, fd_dtype out_dtype, void *out, float *lse,
+                          void *stream);
+
+/* Append one token per sequence [P3 §3.2-3.3, §4.2].
+ *   k_new, v_new  device [B, Hkv, D] in problem.q_dtype for an FD_E4M3 cache
+ *                 (quantised as code = e4m3_rne_satfinite(x / scale[page, kvh]),
+ *                 the division in fp32), otherwise in kv_dtype (bits copied)
+ *   k/v_pages     device pools, modified in place at position seq_lens[b]:
+ *                 page block_table[b][seq_lens[b] / page_size], slot
+ *                 seq_lens[b] % page_size
+ *   k/v_scale     device fp32 [num_pages, Hkv] for FD_E4M3, else NULL
+ *   status_dev    device int32 or NULL: FD_DEV_BAD_PAGE when the target page
+ *                 is out of range (that sequence is skipped)
+ * seq_lens is NOT advanced; the caller adds 1 after the call. */
+fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void *v_new,
+                       void *k_pages, void *v_pages, const float *k_scale,
+                       const float *v_scale, const int32_t *block_table,
+                       const int32_t *seq_lens, int32_t *status_dev, void *stream);
+
+/* Map a device status word to a status code (FD_OK when zero). */
+fd_status fd_status_from_device(int32_t status_word);
+
+/* Static description of a status code. */
+const char *fd_status_string(fd_status status);
+
+/* FD_API_VERSION of the loaded library. */
+int fd_api_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FD_API_H */

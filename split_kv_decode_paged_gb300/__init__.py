@@ -1,0 +1,82 @@
+"""Paged, GQA-shared, split-KV decode attention for GB300 (sm_103a).
+
+The compute lives in libfd.so (CUDA, C ABI in include/fd_api.h); this package
+binds it with ctypes and uses PyTorch only for device memory and streams.
+
+    from split_kv_decode_paged_gb300 import PagedDecoder
+    dec = PagedDecoder.for_pools(q, k_pages, v_pages, block_table, seq_lens_host)
+    out, lse = dec(q, k_pages, v_pages, block_table, seq_lens)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import (FD_BF16, FD_E4M3, FD_F16, FD_F32, FdError, fd_append_kv, fd_decode_paged, fd_merge_states,
+                   fd_plan, fd_status_from_device, fd_status_string, make_problem)
+
+__all__ = ["PagedDecoder", "fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string",
+           "fd_status_from_device", "make_problem", "FdError", "append_kv", "merge_states"]
+
+
+class PagedDecoder:
+    """A plan plus its workspace and device status word.
+
+    The plan is made once from host lengths and reused while every device
+    length stays within plan.capacity_tokens (pass max_seq_len to reserve
+    room for growth).  Calls on one decoder must not overlap on the GPU."""
+
+    def __init__(self, problem, seq_lens_host, device="cuda", **plan_opts):
+        self.problem = problem
+        self.plan = fd_plan(problem, seq_lens_host, **plan_opts)
+        self.device = torch.device(device)
+        nbytes = max(256, int(self.plan.workspace_bytes))
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    @classmethod
+    def for_pools(cls, q, k_pages, v_pages, block_table, seq_lens_host, out_dtype=None, **plan_opts):
+        B, Hq, D = q.shape
+        num_pages, page_size, Hkv, D2 = k_pages.shape
+        if D2 != D:
+            raise ValueError("head dimension of q and the pools differ")
+        prob = make_problem(B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, q.dtype, k_pages.dtype,
+                            out_dtype)
+        return cls(prob, seq_lens_host, device=q.device, **plan_opts)
+
+    def __call__(self, q, k_pages, v_pages, block_table, seq_lens, k_scale=None, v_scale=None, out=None,
+                 lse=None, want_lse=True, stream=None):
+        p = self.problem
+        if out is None:
+            out = torch.empty((p.B, p.Hq, p.D), dtype=_lib.FD_TO_TORCH[p.out_dtype], device=q.device)
+        if lse is None and want_lse:
+            lse = torch.empty((p.B, p.Hq), dtype=torch.float32, device=q.device)
+        fd_decode_paged(self.plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
+                        self.workspace, self.status, stream)
+        return out, lse
+
+    def check(self):
+        """Synchronise and raise FdError if the device reported an error."""
+        word = int(self.status.item())
+        if word:
+            self.status.zero_()
+            self.workspace.zero_()
+            raise FdError(fd_status_from_device(word), "device status")
+
+
+def append_kv(q_dtype, k_new, v_new, k_pages, v_pages, block_table, seq_lens, k_scale=None, v_scale=None,
+              status=None, stream=None):
+    """Write k_new/v_new [B, Hkv, D] at position seq_lens[b]; seq_lens is not advanced."""
+    B, Hkv, D = k_new.shape
+    num_pages, page_size, _, _ = k_pages.shape
+    prob = make_problem(B, Hkv, Hkv, D, page_size, block_table.shape[1], num_pages, q_dtype, k_pages.dtype)
+    fd_append_kv(prob, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, status, stream)
+
+
+def merge_states(o_part, m, d, out_dtype=torch.float32, want_lse=True, stream=None):
+    """Merge partial states o_part [B,Hq,S,D], m/d [B,Hq,S] -> (out [B,Hq,D], lse)."""
+    B, Hq, S, D = o_part.shape
+    out = torch.empty((B, Hq, D), dtype=out_dtype, device=o_part.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=o_part.device) if want_lse else None
+    fd_merge_states(o_part, m, d, out, lse, stream)
+    return out, lse

@@ -1,0 +1,699 @@
+// decode_kernel.cuh -- persistent split-KV paged decode attention for sm_103a.
+//
+// What one launch computes (lpnh.cn "FlashDecoding 核心原理", stages one and
+// two; "FlashDecoding 与 FlashInfer 深度解析" §2.1): for every sequence b and
+// query head hq, softmax(q k^T / sqrt(D)) V over the tokens [0, seq_lens[b])
+// of its KV head kvh = hq / G, plus the log-sum-exp.
+//
+// Work decomposition.  A work item is (sequence b, split s, KV head kvh): the
+// contiguous token range [s*C, min(L_b, (s+1)*C)) of one KV head, with all G
+// query heads of the group packed into the same CTA so each K/V byte is read
+// once (lpnh.cn "进阶突破", KV-reused layout for GQA).  Sequences shorter than
+// one chunk are not split.  Items are numbered b-major (then s, then kvh) and
+// handed out by an atomic counter to a persistent grid.
+//
+// CTA layout: NC consumer warps + 1 producer warp.
+//   producer: claims items, reads the block table a batch of 32 boxes ahead,
+//     and issues TMA tensor loads of K and V boxes (page-size x D slices of
+//     one KV head) into a ring of shared-memory stages, plus one bulk copy of
+//     the item's G query rows; stage hand-off through full/empty mbarriers.
+//   consumers: each warp takes 16 tokens of every stage:
+//     S^T[16 tok x 8 heads] = K[16 x D] . Q^T  (mma.sync m16n8k16, K from
+//     swizzled shared memory via ldmatrix, Q in registers),
+//     online softmax in the exp2 domain, P^T moved into the B operand with
+//     movmatrix, O^T[D x 8] += V^T[D x 16] . P^T (ldmatrix.trans on V).
+//     At the end of an item the warps merge their states through shared
+//     memory; a single-split item writes out/lse, a multi-split item writes
+//     its partial state (unnormalised O, m, d) and the CTA that completes
+//     the last split of a (b, kvh) merges all of them (atomic counter, no
+//     spin-wait), per the merge formula of stage two.
+// FP8 (E4M3) K/V are converted to f16 in registers (exact); the per-(page,
+// KV head) scales multiply the scores and the P.V product.
+#pragma once
+
+#include <float.h>
+#include <math.h>
+
+#include "fd_internal.h"
+#include "ptx.cuh"
+
+namespace fd {
+
+constexpr int kFlagFirst = 1;
+constexpr int kFlagLast = 2;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct StageMeta {
+    int b, kvh, s, t0, nvalid, flags, nsplit, pad;
+    float kscale[kMaxBoxesPerTile];
+    float vscale[kMaxBoxesPerTile];
+};
+
+__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int KV, int D, int NT, int NC>
+struct DecodeShape {
+    static constexpr int E = (KV == KV_E4M3) ? 1 : 2;  // K/V bytes per element
+    static constexpr int RB = D * E;                   // bytes per K/V row
+    static constexpr int SUBROW = RB > 128 ? 128 : RB; // swizzle span (bytes)
+    static constexpr int NHALF = RB / SUBROW;          // sub-row regions per row
+    static constexpr int TILE = NC * kTokensPerWarp;   // tokens per stage
+    static constexpr int QROWS = 8 * NT;               // padded query rows
+    static constexpr int KV_REGION = TILE * RB;
+    static constexpr int Q_REGION = align_up(QROWS * D * 2, 1024);
+    static constexpr int STAGE = 2 * KV_REGION + Q_REGION;
+    static constexpr int SS = D + 4;                   // scratch row stride (floats)
+    // Per-warp O rows; reused for the merge weights (QROWS x kMaxSplits).
+    static constexpr int SCR_O = (NC * QROWS * SS > QROWS * kMaxSplits) ? NC * QROWS * SS : QROWS * kMaxSplits;
+    static constexpr int SCRATCH = SCR_O * 4 + 2 * NC * QROWS * 4 + 16;
+    static constexpr int THREADS = (NC + 1) * 32;
+    static_assert(D == 64 || D == 128, "D");
+    static_assert(SUBROW == 128 || SUBROW == 64, "swizzle span");
+};
+
+// Offset of 16-byte chunk `chunk` of row `row` in a TMA-swizzled region.
+template <int SUBROW>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    if constexpr (SUBROW == 128)
+        return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+    else
+        return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void flag_status(int *status, int bit) {
+    if (status) atomicOr(status, bit);
+}
+
+template <typename T>
+__device__ __forceinline__ T ldcg(const T *p) {
+    return __ldcg(p);
+}
+
+__device__ __forceinline__ void store_out(void *out, size_t idx, float v, int out_dtype) {
+    if (out_dtype == FD_BF16)
+        reinterpret_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+    else if (out_dtype == FD_F16)
+        reinterpret_cast<__half *>(out)[idx] = __float2half_rn(v);
+    else
+        reinterpret_cast<float *>(out)[idx] = v;
+}
+
+// Fused merge of the nsplit partial states of (b, kvh), run by the consumer
+// warps of the CTA that completed the last split.  alpha: >= G*nsplit floats.
+template <int NC>
+__device__ void merge_group(const DecodeParams &p, int b, int kvh, int nsplit, float *alpha, int warp,
+                            int lane, int D) {
+    const int G = p.G, S = p.S;
+    for (int h = warp; h < G; h += NC) {
+        const size_t row = (size_t)b * p.Hq + (size_t)kvh * G + h;
+        const float *pm = p.part_m + row * S;
+        const float *pd = p.part_d + row * S;
+        float mx = -INFINITY;
+        for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, ldcg(pm + s));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.f;
+        for (int s = lane; s < nsplit; s += 32) {
+            const float ms = ldcg(pm + s);
+            const float a = (ms == -INFINITY) ? 0.f : __expf(ms - mx);
+            alpha[h * nsplit + s] = a;
+            sum += a * ldcg(pd + s);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const bool empty = (mx == -INFINITY) || !(sum > 0.f);
+        const float inv = empty ? 0.f : 1.f / sum;
+        for (int s = lane; s < nsplit; s += 32) alpha[h * nsplit + s] *= inv;
+        if (lane == 0 && p.lse) p.lse[row] = empty ? -INFINITY : mx + logf(sum);
+    }
+    named_bar_sync(1, NC * 32);
+    const int tid = warp * 32 + lane;
+    for (int idx = tid; idx < G * D; idx += NC * 32) {
+        const int h = idx / D, d = idx - h * D;
+        const size_t row = (size_t)b * p.Hq + (size_t)kvh * G + h;
+        const float *po = p.part_o + row * S * D + d;
+        float acc = 0.f;
+        for (int s = 0; s < nsplit; ++s) acc += alpha[h * nsplit + s] * ldcg(po + (size_t)s * D);
+        store_out(p.out, row * D + d, acc, p.out_dtype);
+    }
+}
+
+template <int KV, int D, int NT, int NC, bool QBF16>
+__global__ void __launch_bounds__((NC + 1) * 32, 1)
+    fd_split_kv_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                              const __grid_constant__ CUtensorMap tmv) {
+    using Sh = DecodeShape<KV, D, NT, NC>;
+    constexpr int TILE = Sh::TILE, E = Sh::E, SUBROW = Sh::SUBROW, NHALF = Sh::NHALF;
+    constexpr int QROWS = Sh::QROWS, SS = Sh::SS;
+    constexpr bool FP8 = (KV == KV_E4M3);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int NST = p.stages;
+    uint8_t *stages = smem;
+    float *scratch = reinterpret_cast<float *>(stages + (size_t)NST * Sh::STAGE);
+    float *scr_m = scratch + Sh::SCR_O;
+    float *scr_l = scr_m + NC * QROWS;
+    int *scr_flag = reinterpret_cast<int *>(scr_l + NC * QROWS);
+    StageMeta *meta = reinterpret_cast<StageMeta *>(reinterpret_cast<uint8_t *>(scratch) + align_up(Sh::SCRATCH, 128));
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(meta + NST);
+    uint64_t *empty_bar = full_bar + NST;
+    int *prefix = reinterpret_cast<int *>(empty_bar + NST);
+    int *lens = prefix + p.B + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), NC);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == NC) {
+        // ================================================================ producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+        const int B = p.B, Hkv = p.Hkv, C = p.chunk, ps = p.page_size, boxr = p.boxr;
+        const int BPT = TILE / boxr;  // boxes per tile: 1, 2, 4 (or 8)
+        // Item counts per sequence and their prefix sums.
+        int running = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int b = base + lane;
+            int v = 0;
+            if (b < B) {
+                int L = p.seq_lens[b];
+                if (L < 0 || L > p.cap) {
+                    flag_status(p.status, FD_DEV_CAPACITY);
+                    L = L < 0 ? 0 : p.cap;
+                }
+                lens[b] = L;
+                v = (L == 0 ? 1 : (L + C - 1) / C) * Hkv;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (b < B) prefix[b + 1] = running + v;
+            running += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
+        __syncwarp();
+        const int total = running;
+
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        long long n_issued = 0;
+        while (ok) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(p.work_ctr, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            if (item >= total) break;
+            int lo = 0, hi = B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+            }
+            const int b = lo;
+            const int rem = item - prefix[b];
+            const int s = rem / Hkv, kvh = rem - (rem / Hkv) * Hkv;
+            const int L = lens[b];
+            const int nsplit = (prefix[b + 1] - prefix[b]) / Hkv;
+            const int t_begin = s * C;
+            const int t_end = min(L, t_begin + C);
+            const int ntok = max(0, t_end - t_begin);
+            const int ntiles = max(1, (ntok + TILE - 1) / TILE);
+            const int nbox = (ntok + boxr - 1) / boxr;
+            const int box0 = t_begin / boxr;
+            const int32_t *btrow = p.block_table + (size_t)b * p.max_blocks;
+
+            // Page id of box k of this item (-1 past the end; -2 for a
+            // table column out of range).
+            auto page_of = [&](int k) -> int {
+                if (k >= nbox) return -1;
+                const int col = ((box0 + k) * boxr) / ps;
+                if (col >= p.max_blocks) return -2;
+                return __ldg(btrow + col);
+            };
+            int pg_cur = page_of(lane);
+            int pg_nxt = page_of(32 + lane);
+            float ks_cur = 1.f, vs_cur = 1.f;
+            if constexpr (FP8) {
+                if (pg_cur >= 0 && pg_cur < p.num_pages) {
+                    ks_cur = __ldg(p.k_scale + (size_t)pg_cur * Hkv + kvh);
+                    vs_cur = __ldg(p.v_scale + (size_t)pg_cur * Hkv + kvh);
+                }
+            }
+            int batch = 0;
+            for (int j = 0; j < ntiles; ++j) {
+                const int kb = j * BPT;
+                if (kb >= (batch + 1) * 32) {
+                    ++batch;
+                    pg_cur = pg_nxt;
+                    pg_nxt = page_of((batch + 1) * 32 + lane);
+                    if constexpr (FP8) {
+                        if (pg_cur >= 0 && pg_cur < p.num_pages) {
+                            ks_cur = __ldg(p.k_scale + (size_t)pg_cur * Hkv + kvh);
+                            vs_cur = __ldg(p.v_scale + (size_t)pg_cur * Hkv + kvh);
+                        }
+                    }
+                }
+                const int src_lane = (kb + (lane < BPT ? lane : 0)) & 31;
+                const int pg = __shfl_sync(0xffffffffu, pg_cur, src_lane);
+                const float ksc = __shfl_sync(0xffffffffu, ks_cur, src_lane);
+                const float vsc = __shfl_sync(0xffffffffu, vs_cur, src_lane);
+                const bool live = lane < BPT && (kb + lane) < nbox;
+                const bool good = live && pg >= 0 && pg < p.num_pages;
+                if (live && !good) flag_status(p.status, FD_DEV_BAD_PAGE);
+                const unsigned good_mask = __ballot_sync(0xffffffffu, good);
+
+                if (!mbar_wait_bounded(smem_u32(&empty_bar[st]), ph ^ 1u, p.timeout_ns)) {
+                    flag_status(p.status, FD_DEV_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const int t0 = t_begin + j * TILE;
+                const bool load_q = (j == 0) && (ntok > 0);
+                const uint32_t bytes = (uint32_t)__popc(good_mask) * 2u * (uint32_t)(boxr * Sh::RB) +
+                                       (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+                StageMeta *m = &meta[st];
+                if (lane == 0) {
+                    m->b = b; m->kvh = kvh; m->s = s; m->t0 = t0;
+                    m->nvalid = max(0, min(TILE, t_end - t0));
+                    m->flags = (j == 0 ? kFlagFirst : 0) | (j == ntiles - 1 ? kFlagLast : 0);
+                    m->nsplit = nsplit;
+                }
+                if (lane < BPT) {
+                    m->kscale[lane] = ksc;
+                    m->vscale[lane] = vsc;
+                }
+                __syncwarp();
+                const uint32_t fb = smem_u32(&full_bar[st]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+                __syncwarp();
+                uint8_t *sb = stages + (size_t)st * Sh::STAGE;
+                if (load_q && lane == 0) {
+                    const uint8_t *qsrc = reinterpret_cast<const uint8_t *>(p.q) +
+                                          ((size_t)b * p.Hq + (size_t)kvh * p.G) * D * 2;
+                    bulk_load(smem_u32(sb + 2 * Sh::KV_REGION), qsrc, (uint32_t)(p.G * D * 2), fb);
+                }
+                if (good) {
+                    const int tok = (box0 + kb + lane) * boxr;
+                    const int slot = tok % ps;
+#pragma unroll
+                    for (int h = 0; h < NHALF; ++h) {
+                        const uint32_t off = (uint32_t)(h * TILE * SUBROW + lane * boxr * SUBROW);
+                        tma_load_4d(smem_u32(sb + off), &tmk, fb, h * (SUBROW / E), kvh, slot, pg);
+                        tma_load_4d(smem_u32(sb + Sh::KV_REGION + off), &tmv, fb, h * (SUBROW / E), kvh, slot, pg);
+                    }
+                }
+                ++n_issued;
+                if (++st == NST) { st = 0; ph ^= 1u; }
+            }
+        }
+        if (!ok) {
+            // Abort: wait (bounded) for the copies still in flight into the
+            // stages issued most recently before leaving.
+            for (int k = 1; k <= NST && k <= n_issued; ++k) {
+                const int s2 = (st - k + NST) % NST;
+                const uint32_t par = (s2 < st) ? ph : (ph ^ 1u);
+                mbar_wait_bounded(smem_u32(&full_bar[s2]), par, p.timeout_ns);
+            }
+        }
+        // Stop marker for the consumers.
+        if (ok && mbar_wait_bounded(smem_u32(&empty_bar[st]), ph ^ 1u, p.timeout_ns)) {
+            if (lane == 0) {
+                meta[st].b = -1;
+                mbar_arrive(smem_u32(&full_bar[st]));
+            }
+        } else {
+            flag_status(p.status, FD_DEV_TIMEOUT);
+        }
+        // Last producer out resets the work counters for the next launch.
+        if (lane == 0) {
+            __threadfence();
+            const int done = atomicAdd(p.done_ctr, 1);
+            if (done == (int)gridDim.x - 1) {
+                atomicExch(p.work_ctr, 0);
+                atomicExch(p.done_ctr, 0);
+            }
+        }
+        return;
+    }
+
+    // ==================================================================== consumers
+    const int g = lane >> 2, c = lane & 3;
+    constexpr int KT = D / 16;  // k-steps of QK (f16/bf16 path)
+    constexpr int MT = D / 16;  // m-tiles of PV
+    uint32_t qf[KT][NT][2];
+    float o[MT][NT][4];
+    float mrow[NT][2], lrow[NT][2];
+    const float scale_log2 = p.scale_log2;
+
+    int st = 0;
+    uint32_t ph = 0;
+    while (true) {
+        if (!mbar_wait_bounded(smem_u32(&full_bar[st]), ph, p.timeout_ns)) {
+            flag_status(p.status, FD_DEV_TIMEOUT);
+            break;
+        }
+        const StageMeta &mt = meta[st];
+        const int mb = mt.b;
+        if (mb < 0) break;
+        const int flags = mt.flags, nvalid = mt.nvalid;
+        const uint8_t *sb = stages + (size_t)st * Sh::STAGE;
+        const uint32_t kbase = smem_u32(sb), vbase = kbase + Sh::KV_REGION, qbase = kbase + 2 * Sh::KV_REGION;
+
+        if (flags & kFlagFirst) {
+            // Query fragments (B operand of QK), zero for padded heads.
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const bool live_head = (n * 8 + g) < p.G;
+                if constexpr (!FP8) {
+#pragma unroll
+                    for (int kk = 0; kk < KT; kk += 2) {
+                        const int row = n * 8 + (lane & 7);
+                        const int chunk = 2 * kk + (lane >> 3);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(qbase + (uint32_t)(row * D * 2 + chunk * 16), r0, r1, r2, r3);
+                        qf[kk][n][0] = live_head ? r0 : 0u;
+                        qf[kk][n][1] = live_head ? r1 : 0u;
+                        qf[kk + 1][n][0] = live_head ? r2 : 0u;
+                        qf[kk + 1][n][1] = live_head ? r3 : 0u;
+                    }
+                } else {
+                    // f16 fragments in the E4M3 k-order: k-step ks covers
+                    // d = 32*(ks/2) + 16*(ks%2) + {4c..4c+3}.
+                    const int row = n * 8 + g;
+#pragma unroll
+                    for (int ks = 0; ks < KT; ++ks) {
+                        const int d0 = 32 * (ks >> 1) + 16 * (ks & 1) + 4 * c;
+                        const uint2 raw = *reinterpret_cast<const uint2 *>(sb + 2 * Sh::KV_REGION + (row * D + d0) * 2);
+                        uint32_t w0, w1;
+                        if constexpr (QBF16) {
+                            w0 = pack_f16x2(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u));
+                            w1 = pack_f16x2(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+                        } else {
+                            w0 = raw.x;
+                            w1 = raw.y;
+                        }
+                        qf[ks][n][0] = live_head ? w0 : 0u;
+                        qf[ks][n][1] = live_head ? w1 : 0u;
+                    }
+                }
+            }
+#pragma unroll
+            for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) o[mi][n][r] = 0.f;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                mrow[n][0] = mrow[n][1] = -INFINITY;
+                lrow[n][0] = lrow[n][1] = 0.f;
+            }
+        }
+
+        const int nloc = max(0, min(kTokensPerWarp, nvalid - warp * kTokensPerWarp));
+        if (nloc > 0) {
+            const int row_a = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;  // QK: ldmatrix rows
+            const int row_t = warp * 16 + (lane & 7) + (lane >> 4) * 8;        // PV (f16/bf16): .trans rows
+            // ---------------------------------------------------------- S = K Q^T
+            float sacc[NT][4];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sacc[n][r] = 0.f;
+            if constexpr (!FP8) {
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    const int byte = kk * 32;
+                    const int h = byte / SUBROW;
+                    const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_a, chunk), a0, a1, a2, a3);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        if constexpr (KV == KV_BF16)
+                            mma_bf16(sacc[n], a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                        else
+                            mma_f16(sacc[n], a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int jg = 0; jg < D / 32; ++jg) {
+                    const int byte = jg * 32;
+                    const int h = byte / SUBROW;
+                    const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_a, chunk), r0, r1, r2, r3);
+                    const uint32_t a00 = e4m3x2_to_f16x2((uint16_t)(r0 & 0xffff));
+                    const uint32_t a01 = e4m3x2_to_f16x2((uint16_t)(r1 & 0xffff));
+                    const uint32_t a02 = e4m3x2_to_f16x2((uint16_t)(r0 >> 16));
+                    const uint32_t a03 = e4m3x2_to_f16x2((uint16_t)(r1 >> 16));
+                    const uint32_t a10 = e4m3x2_to_f16x2((uint16_t)(r2 & 0xffff));
+                    const uint32_t a11 = e4m3x2_to_f16x2((uint16_t)(r3 & 0xffff));
+                    const uint32_t a12 = e4m3x2_to_f16x2((uint16_t)(r2 >> 16));
+                    const uint32_t a13 = e4m3x2_to_f16x2((uint16_t)(r3 >> 16));
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        mma_f16(sacc[n], a00, a01, a02, a03, qf[2 * jg][n][0], qf[2 * jg][n][1]);
+                        mma_f16(sacc[n], a10, a11, a12, a13, qf[2 * jg + 1][n][0], qf[2 * jg + 1][n][1]);
+                    }
+                }
+            }
+
+            // ------------------------------------------------- online softmax (exp2)
+            float sc = scale_log2;
+            if constexpr (FP8) sc *= mt.kscale[(warp * kTokensPerWarp) / p.boxr];
+            const bool v0 = g < nloc, v1 = (g + 8) < nloc;
+            float alpha[NT][2];
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const float s0 = v0 ? sacc[n][0] * sc : -INFINITY;
+                const float s1 = v0 ? sacc[n][1] * sc : -INFINITY;
+                const float s2 = v1 ? sacc[n][2] * sc : -INFINITY;
+                const float s3 = v1 ? sacc[n][3] * sc : -INFINITY;
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, shfl_xor(mx0, off));
+                    mx1 = fmaxf(mx1, shfl_xor(mx1, off));
+                }
+                const float mn0 = fmaxf(mrow[n][0], mx0), mn1 = fmaxf(mrow[n][1], mx1);
+                alpha[n][0] = (mn0 == -INFINITY) ? 1.f : ex2(mrow[n][0] - mn0);
+                alpha[n][1] = (mn1 == -INFINITY) ? 1.f : ex2(mrow[n][1] - mn1);
+                mrow[n][0] = mn0;
+                mrow[n][1] = mn1;
+                const float p0 = (mn0 == -INFINITY) ? 0.f : ex2(s0 - mn0);
+                const float p1 = (mn1 == -INFINITY) ? 0.f : ex2(s1 - mn1);
+                const float p2 = (mn0 == -INFINITY) ? 0.f : ex2(s2 - mn0);
+                const float p3 = (mn1 == -INFINITY) ? 0.f : ex2(s3 - mn1);
+                uint32_t x0, x1;
+                float r0, r1, r2, r3;  // the rounded weights actually used
+                if constexpr (KV == KV_BF16) {
+                    x0 = pack_bf16x2(p0, p1);
+                    x1 = pack_bf16x2(p2, p3);
+                    r0 = __uint_as_float(x0 << 16); r1 = __uint_as_float(x0 & 0xffff0000u);
+                    r2 = __uint_as_float(x1 << 16); r3 = __uint_as_float(x1 & 0xffff0000u);
+                } else {
+                    x0 = pack_f16x2(p0, p1);
+                    x1 = pack_f16x2(p2, p3);
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&x0));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&x1));
+                    r0 = f0.x; r1 = f0.y; r2 = f1.x; r3 = f1.y;
+                }
+                lrow[n][0] = lrow[n][0] * alpha[n][0] + (r0 + r2);
+                lrow[n][1] = lrow[n][1] * alpha[n][1] + (r1 + r3);
+                pb[n][0] = movmatrix_t(x0);
+                pb[n][1] = movmatrix_t(x1);
+            }
+#pragma unroll
+            for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    o[mi][n][0] *= alpha[n][0];
+                    o[mi][n][1] *= alpha[n][1];
+                    o[mi][n][2] *= alpha[n][0];
+                    o[mi][n][3] *= alpha[n][1];
+                }
+
+            // ---------------------------------------------------- O^T += V^T P^T
+            uint32_t msk01 = 0xffffffffu, msk23 = 0xffffffffu;
+            if (nloc < kTokensPerWarp) {
+                msk01 = ((2 * c) < nloc ? 0x0000ffffu : 0u) | ((2 * c + 1) < nloc ? 0xffff0000u : 0u);
+                msk23 = ((2 * c + 8) < nloc ? 0x0000ffffu : 0u) | ((2 * c + 9) < nloc ? 0xffff0000u : 0u);
+            }
+            if constexpr (!FP8) {
+#pragma unroll
+                for (int mi = 0; mi < MT; ++mi) {
+                    const int byte = mi * 32;
+                    const int h = byte / SUBROW;
+                    const int chunk = (byte % SUBROW) / 16 + ((lane >> 3) & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_t, chunk), a0, a1, a2, a3);
+                    a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        if constexpr (KV == KV_BF16)
+                            mma_bf16(o[mi][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+                        else
+                            mma_f16(o[mi][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+                    }
+                }
+            } else {
+                const float vsc = mt.vscale[(warp * kTokensPerWarp) / p.boxr];
+#pragma unroll
+                for (int jg = 0; jg < D / 32; ++jg) {
+                    const int byte = jg * 32;
+                    const int h = byte / SUBROW;
+                    const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(vbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_a, chunk), r0, r1, r2, r3);
+                    const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
+                    const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
+                    uint32_t A[2][4];
+                    A[0][0] = e4m3x2_to_f16x2((uint16_t)(t0 & 0xffff)) & msk01;
+                    A[0][1] = e4m3x2_to_f16x2((uint16_t)(t0 >> 16)) & msk01;
+                    A[0][2] = e4m3x2_to_f16x2((uint16_t)(t1 & 0xffff)) & msk23;
+                    A[0][3] = e4m3x2_to_f16x2((uint16_t)(t1 >> 16)) & msk23;
+                    A[1][0] = e4m3x2_to_f16x2((uint16_t)(t2 & 0xffff)) & msk01;
+                    A[1][1] = e4m3x2_to_f16x2((uint16_t)(t2 >> 16)) & msk01;
+                    A[1][2] = e4m3x2_to_f16x2((uint16_t)(t3 & 0xffff)) & msk23;
+                    A[1][3] = e4m3x2_to_f16x2((uint16_t)(t3 >> 16)) & msk23;
+#pragma unroll
+                    for (int hs = 0; hs < 2; ++hs)
+#pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_f16(acc, A[hs][0], A[hs][1], A[hs][2], A[hs][3], pb[n][0], pb[n][1]);
+                            float *od = o[2 * jg + hs][n];
+                            od[0] = fmaf(acc[0], vsc, od[0]);
+                            od[1] = fmaf(acc[1], vsc, od[1]);
+                            od[2] = fmaf(acc[2], vsc, od[2]);
+                            od[3] = fmaf(acc[3], vsc, od[3]);
+                        }
+                }
+            }
+        }
+        // Release the stage (all reads of it are done).
+        const int m_kvh = mt.kvh, m_s = mt.s, m_nsplit = mt.nsplit;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+        if (++st == NST) { st = 0; ph ^= 1u; }
+        if (!(flags & kFlagLast)) continue;
+
+        // ========================================================== item epilogue
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float v = lrow[n][r];
+                v += shfl_xor(v, 4);
+                v += shfl_xor(v, 8);
+                v += shfl_xor(v, 16);
+                lrow[n][r] = v;
+            }
+        float *so = scratch + warp * QROWS * SS;
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+            const int d0 = FP8 ? 16 * mi + 2 * g : 16 * mi + g;
+            const int d1 = FP8 ? d0 + 1 : d0 + 8;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int h0 = n * 8 + 2 * c, h1 = h0 + 1;
+                so[h0 * SS + d0] = o[mi][n][0];
+                so[h1 * SS + d0] = o[mi][n][1];
+                so[h0 * SS + d1] = o[mi][n][2];
+                so[h1 * SS + d1] = o[mi][n][3];
+            }
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int h0 = n * 8 + 2 * c;
+                scr_m[warp * QROWS + h0] = mrow[n][0];
+                scr_m[warp * QROWS + h0 + 1] = mrow[n][1];
+                scr_l[warp * QROWS + h0] = lrow[n][0];
+                scr_l[warp * QROWS + h0 + 1] = lrow[n][1];
+            }
+        }
+        named_bar_sync(1, NC * 32);
+        const int tid = warp * 32 + lane;
+        const int G = p.G;
+        for (int idx = tid; idx < G * D; idx += NC * 32) {
+            const int h = idx / D, d = idx - h * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) M = fmaxf(M, scr_m[w * QROWS + h]);
+            float acc = 0.f, Ls = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < NC; ++w) {
+                    const float a = ex2(scr_m[w * QROWS + h] - M);
+                    acc += a * scratch[(w * QROWS + h) * SS + d];
+                    Ls += a * scr_l[w * QROWS + h];
+                }
+            }
+            const size_t row = (size_t)mb * p.Hq + (size_t)m_kvh * G + h;
+            if (m_nsplit == 1) {
+                const bool empty = !(Ls > 0.f);
+                store_out(p.out, row * D + d, empty ? 0.f : acc / Ls, p.out_dtype);
+                if (d == 0 && p.lse) p.lse[row] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+            } else {
+                p.part_o[(row * p.S + m_s) * D + d] = acc;
+                if (d == 0) {
+                    p.part_m[row * p.S + m_s] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+                    p.part_d[row * p.S + m_s] = Ls;
+                }
+            }
+        }
+        if (m_nsplit > 1 && p.fuse_merge) {
+            __threadfence();
+            named_bar_sync(1, NC * 32);
+            if (tid == 0) {
+                const int prev = atomicAdd(p.merge_ctr + (size_t)mb * p.Hkv + m_kvh, 1);
+                *scr_flag = (prev == m_nsplit - 1);
+            }
+            named_bar_sync(1, NC * 32);
+            if (*scr_flag) {
+                __threadfence();
+                merge_group<NC>(p, mb, m_kvh, m_nsplit, scratch, warp, lane, D);
+                if (tid == 0) atomicExch(p.merge_ctr + (size_t)mb * p.Hkv + m_kvh, 0);
+            }
+        }
+        named_bar_sync(1, NC * 32);
+    }
+}
+
+template <int KV, int D, int NT, int NC, bool QBF16>
+size_t decode_smem_for(int stages, int B) {
+    using Sh = DecodeShape<KV, D, NT, NC>;
+    size_t n = 1024;  // alignment slack
+    n += (size_t)stages * Sh::STAGE;
+    n += align_up(Sh::SCRATCH, 128);
+    n += (size_t)stages * sizeof(StageMeta);
+    n += (size_t)stages * 16;
+    n += (size_t)(2 * B + 1) * 4;
+    return n;
+}
+
+template <int KV, int D, int NT, int NC, bool QBF16>
+cudaError_t launch_decode_t(const DecodeParams &dp, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                            size_t smem, cudaStream_t stream) {
+    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, QBF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, DecodeShape<KV, D, NT, NC>::THREADS, smem, stream>>>(dp, tmk, tmv);
+    return cudaGetLastError();
+}
+
+}  // namespace fd

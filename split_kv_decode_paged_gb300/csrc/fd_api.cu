@@ -1,0 +1,480 @@
+// fd_api.cu -- the C ABI of libfd (declared in include/fd_api.h): problem
+// validation, the split-count cost model, TMA descriptor encoding and the
+// kernel launches.  No device memory is allocated here.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <queue>
+#include <vector>
+
+#include "fd_internal.h"
+
+namespace fd {
+
+cudaError_t launch_decode_f16(const fd_problem &, const KernelShape &, const DecodeParams &, const CUtensorMap &,
+                              const CUtensorMap &, int, size_t, cudaStream_t);
+cudaError_t launch_decode_bf16(const fd_problem &, const KernelShape &, const DecodeParams &, const CUtensorMap &,
+                               const CUtensorMap &, int, size_t, cudaStream_t);
+cudaError_t launch_decode_e4m3(const fd_problem &, const KernelShape &, const DecodeParams &, const CUtensorMap &,
+                               const CUtensorMap &, int, size_t, cudaStream_t);
+size_t decode_smem_f16(const fd_problem &, const KernelShape &, int);
+size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int);
+size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
+
+KernelShape kernel_shape(const fd_problem &p) {
+    KernelShape ks;
+    ks.consumer_warps = 4;
+    ks.tile = ks.consumer_warps * kTokensPerWarp;
+    ks.nt = (p.Hq / p.Hkv) <= 8 ? 1 : 2;
+    return ks;
+}
+
+size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages) {
+    switch (p.kv_dtype) {
+    case FD_F16: return decode_smem_f16(p, ks, stages);
+    case FD_BF16: return decode_smem_bf16(p, ks, stages);
+    default: return decode_smem_e4m3(p, ks, stages);
+    }
+}
+
+cudaError_t launch_decode(const fd_problem &p, const KernelShape &ks, const DecodeParams &dp, const CUtensorMap &tmk,
+                          const CUtensorMap &tmv, int grid, size_t smem, cudaStream_t stream) {
+    switch (p.kv_dtype) {
+    case FD_F16: return launch_decode_f16(p, ks, dp, tmk, tmv, grid, smem, stream);
+    case FD_BF16: return launch_decode_bf16(p, ks, dp, tmk, tmv, grid, smem, stream);
+    default: return launch_decode_e4m3(p, ks, dp, tmk, tmv, grid, smem, stream);
+    }
+}
+
+}  // namespace fd
+
+using namespace fd;
+
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kMinStages = 2;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s limit on any device-side wait
+// Cost-model constants (in token-times of one CTA): fixed cost of one work
+// item (epilogue + pipeline hand-over) and the relative margin within which
+// fewer splits are preferred.
+constexpr double kItemOverheadTokens = 48.0;
+constexpr int kDefaultSplitMarginPct = 2;
+
+int elem_bytes(fd_dtype t) { return t == FD_E4M3 ? 1 : (t == FD_F32 ? 4 : 2); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+fd_status validate_problem(const fd_problem *p) {
+    if (!p) return FD_ERR_INVALID_ARG;
+    if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->D < 1 || p->page_size < 1 || p->max_blocks_per_seq < 1 ||
+        p->num_pages < 1)
+        return FD_ERR_INVALID_ARG;
+    if (p->Hq % p->Hkv != 0) return FD_ERR_INVALID_ARG;
+    if (p->page_size % 16 != 0) return FD_ERR_INVALID_ARG;
+    if (p->q_dtype != FD_F16 && p->q_dtype != FD_BF16) return FD_ERR_UNSUPPORTED;
+    if (p->kv_dtype == FD_E4M3) {
+        // q may be f16 or bf16
+    } else if (p->kv_dtype != p->q_dtype) {
+        return FD_ERR_UNSUPPORTED;
+    }
+    if (p->out_dtype != p->q_dtype && p->out_dtype != FD_F32) return FD_ERR_UNSUPPORTED;
+    if (p->D != 64 && p->D != 128) return FD_ERR_UNSUPPORTED;
+    if (p->Hq / p->Hkv > 16) return FD_ERR_UNSUPPORTED;
+    if (p->B > kMaxBatch) return FD_ERR_UNSUPPORTED;
+    if ((long long)p->page_size * p->max_blocks_per_seq > (1LL << 30)) return FD_ERR_UNSUPPORTED;
+    return FD_OK;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+fd_status device_info(DeviceInfo &di) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FD_ERR_CUDA;
+    static std::mutex mu;
+    static std::vector<DeviceInfo> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1);
+    if (cache[dev].sms == 0) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FD_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return FD_ERR_CUDA;
+        cache[dev] = d;
+    }
+    di = cache[dev];
+    return FD_OK;
+}
+
+int round_up(long long x, int a) { return (int)(((x + a - 1) / a) * a); }
+
+// Greedy list-scheduling estimate of the busiest CTA (in token-times) when
+// the items of chunk length C are handed out in b-major order to P CTAs.
+double makespan(const std::vector<int> &lens, int Hkv, int C, int P, double item_ovh) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> q;
+    for (int i = 0; i < P; ++i) q.push(0.0);
+    double worst = 0.0;
+    for (int L : lens) {
+        const int n = L == 0 ? 1 : (L + C - 1) / C;
+        for (int s = 0; s < n; ++s) {
+            const int len = std::max(0, std::min(C, L - s * C));
+            for (int h = 0; h < Hkv; ++h) {
+                double t = q.top();
+                q.pop();
+                t += len + item_ovh;
+                worst = std::max(worst, t);
+                q.push(t);
+            }
+        }
+    }
+    return worst;
+}
+
+// The pages' split rule (lpnh.cn "进阶突破": a cost model over batch, heads,
+// length and SM count, no split for short sequences; "Inference Cookbook"
+// §6.3: no split when the batch already fills the SMs, otherwise the fewest
+// splits whose efficiency is close to the best).  Returns the chunk length.
+int choose_chunk(const std::vector<int> &lens, const fd_problem &p, int P, int tile, double margin) {
+    const int maxL = *std::max_element(lens.begin(), lens.end());
+    const int G = p.Hq / p.Hkv;
+    if (maxL <= 2 * kMinChunkTokens) return std::max(tile, round_up(std::max(maxL, 1), tile));
+    const long long W = (long long)p.B * p.Hkv;
+    std::vector<int> cand;
+    for (int s = 1; s <= 64; ++s) cand.push_back(s);
+    for (int k = 1; k <= 8; ++k) cand.push_back((int)((k * (long long)P + W - 1) / W));
+    std::sort(cand.begin(), cand.end());
+    cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
+    struct Opt { int S, C; double cost; };
+    std::vector<Opt> opts;
+    int lastC = -1;
+    for (int S : cand) {
+        if (S < 1 || S > kMaxSplits) continue;
+        const int C = std::max(tile, round_up((maxL + S - 1) / S, tile));
+        if (C == lastC) continue;
+        if (S > 1 && C < kMinChunkTokens) break;
+        lastC = C;
+        long long items = 0;
+        for (int L : lens) items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv;
+        if (S > 1 && items > 16LL * P) continue;
+        const int nmax = (maxL + C - 1) / C;
+        double cost = makespan(lens, p.Hkv, C, P, kItemOverheadTokens);
+        if (nmax > 1) cost += 0.5 * G * nmax;  // merge of nmax partials by one CTA
+        opts.push_back({S, C, cost});
+    }
+    if (opts.empty()) return std::max(tile, round_up(maxL, tile));
+    double best = opts[0].cost;
+    for (auto &o : opts) best = std::min(best, o.cost);
+    // Largest chunk (fewest splits) within the margin of the best.
+    int bestC = opts[0].C;
+    for (auto &o : opts)
+        if (o.cost <= best * (1.0 + margin)) { bestC = o.C; break; }
+    return bestC;
+}
+
+// ------------------------------------------------------- tensor map encoding
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// K or V pool viewed as (D, Hkv, page_size, num_pages); one box = `boxr`
+// token rows x one swizzle span of D for a single KV head.
+bool encode_pool_map(CUtensorMap *map, const void *pool, const fd_problem &p, int boxr) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int e = elem_bytes(p.kv_dtype);
+    const int rb = p.D * e;
+    const int span = rb > 128 ? 128 : rb;
+    cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.Hkv, (cuuint64_t)p.page_size, (cuuint64_t)p.num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)rb, (cuuint64_t)rb * p.Hkv, (cuuint64_t)rb * p.Hkv * p.page_size};
+    cuuint32_t box[4] = {(cuuint32_t)(span / e), 1u, (cuuint32_t)boxr, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapDataType dt = e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUresult r = fn(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_api_version(void) { return FD_API_VERSION; }
+
+const char *fd_status_string(fd_status s) {
+    switch (s) {
+    case FD_OK: return "ok";
+    case FD_ERR_INVALID_ARG: return "invalid argument";
+    case FD_ERR_UNSUPPORTED: return "unsupported problem";
+    case FD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FD_ERR_BAD_PAGE: return "block-table entry out of range";
+    case FD_ERR_CUDA: return "CUDA error";
+    case FD_ERR_CAPACITY: return "sequence length above the plan capacity";
+    case FD_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+fd_status fd_status_from_device(int32_t w) {
+    if (w & FD_DEV_TIMEOUT) return FD_ERR_TIMEOUT;
+    if (w & FD_DEV_BAD_PAGE) return FD_ERR_BAD_PAGE;
+    if (w & FD_DEV_CAPACITY) return FD_ERR_CAPACITY;
+    return FD_OK;
+}
+
+fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const fd_plan_options *options,
+                  fd_plan_t *plan) {
+    if (!plan || !seq_lens_host) return FD_ERR_INVALID_ARG;
+    fd_status st = validate_problem(problem);
+    if (st != FD_OK) return st;
+    fd_plan_options opt = {0, 0, 1, 0, 0, 0};
+    if (options) opt = *options;
+    if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 ||
+        opt.split_margin_pct < 0 || opt.split_margin_pct > 100)
+        return FD_ERR_INVALID_ARG;
+    const double margin = (opt.split_margin_pct > 0 ? opt.split_margin_pct : kDefaultSplitMarginPct) / 100.0;
+    const fd_problem &p = *problem;
+    std::vector<int> lens(p.B);
+    long long maxL = 0;
+    for (int b = 0; b < p.B; ++b) {
+        if (seq_lens_host[b] < 0) return FD_ERR_INVALID_ARG;
+        lens[b] = seq_lens_host[b];
+        maxL = std::max<long long>(maxL, lens[b]);
+    }
+    const long long capL = std::max<long long>(maxL, opt.max_seq_len);
+    if (capL > (long long)p.page_size * p.max_blocks_per_seq) return FD_ERR_INVALID_ARG;
+
+    // The device is queried when present; planning for an explicit SM count
+    // also works on a host without a GPU (shared memory then assumes 227 KB).
+    DeviceInfo di;
+    int sms = opt.num_sms;
+    int smem_optin = 232448;
+    st = device_info(di);
+    if (st == FD_OK) smem_optin = di.smem_optin;
+    if (sms == 0) {
+        if (st != FD_OK) return st;
+        sms = di.sms;
+    }
+    const KernelShape ks = kernel_shape(p);
+    const int tile = ks.tile;
+    const int ctas_per_sm = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
+    const int P = sms * ctas_per_sm;
+
+    int C;
+    if (opt.num_splits > 0) {
+        const int S = std::min(opt.num_splits, kMaxSplits);
+        C = std::max(tile, round_up((std::max<long long>(maxL, 1) + S - 1) / S, tile));
+    } else {
+        C = choose_chunk(lens, p, P, tile, margin);
+    }
+    int slots = (int)std::max<long long>(1, (capL + C - 1) / C);
+    if (slots > kMaxSplits) {
+        C = std::max(tile, round_up((capL + kMaxSplits - 1) / kMaxSplits, tile));
+        slots = (int)std::max<long long>(1, (capL + C - 1) / C);
+    }
+    long long items = 0;
+    for (int L : lens) items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv;
+
+    // Deepest pipeline that fits in shared memory.
+    int stages = 0;
+    size_t smem = 0;
+    for (int s = kMaxStages; s >= kMinStages; --s) {
+        const size_t need = decode_smem_bytes(p, ks, s);
+        if ((long long)need <= smem_optin / ctas_per_sm) {
+            stages = s;
+            smem = need;
+            break;
+        }
+    }
+    if (stages == 0) return FD_ERR_UNSUPPORTED;
+
+    std::memset(plan, 0, sizeof(*plan));
+    plan->problem = p;
+    plan->num_splits = slots;
+    plan->chunk_tokens = C;
+    plan->tile_tokens = tile;
+    plan->capacity_tokens = slots * C;
+    plan->grid_ctas = (int)std::max<long long>(1, std::min<long long>(P, items));
+    plan->num_sms = sms;
+    plan->fuse_merge = opt.fuse_merge ? 1 : 0;
+    plan->stages = stages;
+    plan->smem_bytes = (int)smem;
+    plan->work_items_hint = items;
+    const size_t rows = (size_t)p.B * p.Hq;
+    size_t off = 0;
+    plan->ws_partial_o = off;
+    off += align256(slots > 1 ? rows * slots * p.D * sizeof(float) : 0);
+    plan->ws_partial_md = off;
+    off += align256(slots > 1 ? 2 * rows * slots * sizeof(float) : 0);
+    plan->ws_counters = off;
+    off += align256(((size_t)p.B * p.Hkv + 2) * sizeof(int));
+    plan->workspace_bytes = off;
+    return FD_OK;
+}
+
+fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pages, const void *v_pages,
+                          const float *k_scale, const float *v_scale, const int32_t *block_table,
+                          const int32_t *seq_lens, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                          int32_t *status_dev, void *stream) {
+    if (!plan) return FD_ERR_INVALID_ARG;
+    const fd_problem &p = plan->problem;
+    fd_status st = validate_problem(&p);
+    if (st != FD_OK) return st;
+    if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out || !workspace) return FD_ERR_INVALID_ARG;
+    const bool fp8 = p.kv_dtype == FD_E4M3;
+    if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return FD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 256) || (lse && !aligned(lse, 4)) || (k_scale && !aligned(k_scale, 4)) ||
+        (v_scale && !aligned(v_scale, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return FD_ERR_INVALID_ARG;
+    if (workspace_bytes < plan->workspace_bytes) return FD_ERR_WORKSPACE_TOO_SMALL;
+    const KernelShape ks = kernel_shape(p);
+    if (plan->tile_tokens != ks.tile || plan->chunk_tokens < ks.tile || plan->chunk_tokens % ks.tile != 0 ||
+        plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->stages < kMinStages ||
+        plan->stages > kMaxStages || plan->grid_ctas < 1)
+        return FD_ERR_INVALID_ARG;
+
+    const int boxr = std::gcd(p.page_size, ks.tile);
+    CUtensorMap tmk, tmv;
+    if (!encode_pool_map(&tmk, k_pages, p, boxr) || !encode_pool_map(&tmv, v_pages, p, boxr)) return FD_ERR_CUDA;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t rows = (size_t)p.B * p.Hq;
+    DecodeParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    dp.q = q;
+    dp.block_table = block_table;
+    dp.seq_lens = seq_lens;
+    dp.k_scale = k_scale;
+    dp.v_scale = v_scale;
+    dp.out = out;
+    dp.lse = lse;
+    dp.part_o = reinterpret_cast<float *>(ws + plan->ws_partial_o);
+    dp.part_m = reinterpret_cast<float *>(ws + plan->ws_partial_md);
+    dp.part_d = dp.part_m + rows * plan->num_splits;
+    int *ctr = reinterpret_cast<int *>(ws + plan->ws_counters);
+    dp.merge_ctr = ctr;
+    dp.work_ctr = ctr + (size_t)p.B * p.Hkv;
+    dp.done_ctr = dp.work_ctr + 1;
+    dp.status = status_dev;
+    dp.B = p.B;
+    dp.Hq = p.Hq;
+    dp.Hkv = p.Hkv;
+    dp.G = p.Hq / p.Hkv;
+    dp.page_size = p.page_size;
+    dp.max_blocks = p.max_blocks_per_seq;
+    dp.num_pages = p.num_pages;
+    dp.S = plan->num_splits;
+    dp.chunk = plan->chunk_tokens;
+    dp.cap = plan->num_splits * plan->chunk_tokens;
+    dp.boxr = boxr;
+    dp.out_dtype = p.out_dtype;
+    dp.fuse_merge = plan->fuse_merge;
+    dp.stages = plan->stages;
+    dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
+    dp.timeout_ns = kTimeoutNs;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode(p, ks, dp, tmk, tmv, plan->grid_ctas, (size_t)plan->smem_bytes, s);
+    if (e != cudaSuccess) return FD_ERR_CUDA;
+    if (!plan->fuse_merge && plan->num_splits > 1) {
+        MergeParams mp;
+        mp.part_o = dp.part_o;
+        mp.part_m = dp.part_m;
+        mp.part_d = dp.part_d;
+        mp.out = out;
+        mp.lse = lse;
+        mp.seq_lens = seq_lens;
+        mp.B = p.B;
+        mp.Hq = p.Hq;
+        mp.S = plan->num_splits;
+        mp.D = p.D;
+        mp.chunk = plan->chunk_tokens;
+        mp.cap = dp.cap;
+        mp.out_dtype = p.out_dtype;
+        e = launch_merge(mp, s);
+        if (e != cudaSuccess) return FD_ERR_CUDA;
+    }
+    return FD_OK;
+}
+
+fd_status fd_merge_states(const float *o_part, const float *m, const float *d, int B, int Hq, int S, int D,
+                          fd_dtype out_dtype, void *out, float *lse, void *stream) {
+    if (!o_part || !m || !d || !out) return FD_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || S < 1 || D < 1) return FD_ERR_INVALID_ARG;
+    if (S > 4096 || D > 256) return FD_ERR_UNSUPPORTED;
+    if (out_dtype != FD_F16 && out_dtype != FD_BF16 && out_dtype != FD_F32) return FD_ERR_UNSUPPORTED;
+    if (!aligned(o_part, 4) || !aligned(m, 4) || !aligned(d, 4) || !aligned(out, elem_bytes(out_dtype)) ||
+        (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    MergeParams mp;
+    mp.part_o = o_part;
+    mp.part_m = m;
+    mp.part_d = d;
+    mp.out = out;
+    mp.lse = lse;
+    mp.seq_lens = nullptr;
+    mp.B = B;
+    mp.Hq = Hq;
+    mp.S = S;
+    mp.D = D;
+    mp.chunk = 1;
+    mp.cap = 0;
+    mp.out_dtype = out_dtype;
+    return launch_merge(mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void *v_new, void *k_pages,
+                       void *v_pages, const float *k_scale, const float *v_scale, const int32_t *block_table,
+                       const int32_t *seq_lens, int32_t *status_dev, void *stream) {
+    fd_status st = validate_problem(problem);
+    if (st != FD_OK) return st;
+    const fd_problem &p = *problem;
+    if (!k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens) return FD_ERR_INVALID_ARG;
+    const bool fp8 = p.kv_dtype == FD_E4M3;
+    if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return FD_ERR_INVALID_ARG;
+    if (!aligned(k_new, 4) || !aligned(v_new, 4) || !aligned(k_pages, 4) || !aligned(v_pages, 4))
+        return FD_ERR_INVALID_ARG;
+    AppendParams ap;
+    ap.k_new = k_new;
+    ap.v_new = v_new;
+    ap.k_pages = k_pages;
+    ap.v_pages = v_pages;
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
+    ap.block_table = block_table;
+    ap.seq_lens = seq_lens;
+    ap.status = status_dev;
+    ap.B = p.B;
+    ap.Hkv = p.Hkv;
+    ap.D = p.D;
+    ap.page_size = p.page_size;
+    ap.max_blocks = p.max_blocks_per_seq;
+    ap.num_pages = p.num_pages;
+    ap.kv_kind = p.kv_dtype == FD_F16 ? KV_F16 : (p.kv_dtype == FD_BF16 ? KV_BF16 : KV_E4M3);
+    ap.new_is_bf16 = p.q_dtype == FD_BF16 ? 1 : 0;
+    return launch_append(ap, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // extern "C"

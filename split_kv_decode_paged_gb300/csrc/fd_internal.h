@@ -1,0 +1,89 @@
+// fd_internal.h -- parameters shared between the C ABI layer (fd_api.cu) and
+// the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fd_api.h"
+
+namespace fd {
+
+// Consumer warps per CTA, tokens per consumer warp per stage, and the
+// pipeline tile (tokens per stage) that follows from them.
+constexpr int kTokensPerWarp = 16;
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kMaxBoxesPerTile = 8;
+constexpr int kMaxSplits = 512;      // partial slots per (b, hq)
+constexpr int kMaxBatch = 8192;
+constexpr int kMinChunkTokens = 256; // below this a sequence is not split
+
+enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+
+struct DecodeParams {
+    const void *q;             // [B, Hq, D]
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const float *k_scale;      // [num_pages, Hkv] or null
+    const float *v_scale;
+    void *out;                 // [B, Hq, D]
+    float *lse;                // [B, Hq] or null
+    float *part_o;             // [B, Hq, S, D]
+    float *part_m;             // [B, Hq, S]
+    float *part_d;             // [B, Hq, S]
+    int *merge_ctr;            // [B, Hkv]
+    int *work_ctr;             // 1
+    int *done_ctr;             // 1
+    int *status;               // null allowed
+    int B, Hq, Hkv, G;
+    int page_size, max_blocks, num_pages;
+    int S;                     // partial slots per (b, hq)
+    int chunk;                 // tokens per split
+    int cap;                   // S * chunk
+    int boxr;                  // token rows per TMA box: gcd(page_size, tile)
+    int out_dtype;             // fd_dtype
+    int fuse_merge;
+    int stages;
+    float scale_log2;          // log2(e) / sqrt(D)
+    uint64_t timeout_ns;
+};
+
+struct MergeParams {
+    const float *part_o, *part_m, *part_d;
+    void *out;
+    float *lse;
+    const int32_t *seq_lens;   // non-null: per-sequence split counts from lengths
+    int B, Hq, S, D, chunk, cap;
+    int out_dtype;
+};
+
+struct AppendParams {
+    const void *k_new, *v_new;
+    void *k_pages, *v_pages;
+    const float *k_scale, *v_scale;
+    const int32_t *block_table, *seq_lens;
+    int *status;
+    int B, Hkv, D, page_size, max_blocks, num_pages;
+    int kv_kind;               // KvKind
+    int new_is_bf16;           // for E4M3 caches: input dtype bf16 (1) or f16 (0)
+};
+
+// Kernel configuration chosen at plan time.
+struct KernelShape {
+    int consumer_warps;  // 4 or 8
+    int tile;            // consumer_warps * kTokensPerWarp
+    int nt;              // 8-wide head tiles: 1 (G <= 8) or 2 (G <= 16)
+};
+
+KernelShape kernel_shape(const fd_problem &p);
+size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages);
+int decode_max_stages(const fd_problem &p, const KernelShape &ks);
+
+cudaError_t launch_decode(const fd_problem &p, const KernelShape &ks, const DecodeParams &dp,
+                          const CUtensorMap &tmk, const CUtensorMap &tmv, int grid, size_t smem,
+                          cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams &mp, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams &ap, cudaStream_t stream);
+
+}  // namespace fd

@@ -29,3 +29,12 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def fdlib():
+    """Build (if needed) and load libfd.so; fail loudly when it cannot load."""
+    from split_kv_decode_paged_gb300 import build as fd_build
+    from split_kv_decode_paged_gb300 import _lib
+    fd_build.build()
+    return _lib.load()

@@ -1,0 +1,221 @@
+"""GPU parity tests: the CUDA decode path (through the C ABI) against the fp64
+oracle on the same seeded inputs, plus bit-exact paging and device-error
+reporting.  Bars: out max-abs <= 2e-3 and lse <= 1e-3 for f16/bf16 K/V,
+out <= 3e-2 for E4M3 K/V (oracle on the dequantised stored values)."""
+import numpy as np
+import pytest
+import torch
+
+import split_kv_decode_paged_gb300 as fd
+from split_kv_decode_paged_gb300 import _lib
+from split_kv_decode_paged_gb300 import workloads as W
+from tests.gpu_helpers import (TOL_OUT, assert_close, gpu_decode, oracle_full, oracle_pairs)
+
+pytestmark = pytest.mark.gpu
+
+
+def _spec(name, B, Hq, Hkv, D, ps, kv, q, lens, pool=("factor", 1.5), k_mult=1.0, extra_blocks=0):
+    return W.Spec(name, B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=ps, kv=kv, q=q, lens=("list", list(lens)),
+                  pool=pool, k_mult=k_mult, extra_blocks=extra_blocks)
+
+
+def _run_and_check(spec, seed, out_dtype=None, **plan_opts):
+    wl = W.make(spec, seed, "cpu")
+    out, lse, dec = gpu_decode(wl.to("cuda"), out_dtype=out_dtype, **plan_opts)
+    ref_o, ref_l = oracle_full(wl)
+    err = assert_close(spec.kv, out, lse, ref_o, ref_l, what=f"{spec.name} {plan_opts}")
+    return err, dec
+
+
+@pytest.mark.parametrize("fuse", [1, 0])
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 7])
+def test_tiny_mha_forced_splits(fdlib, splits, fuse):
+    spec = W.CONFIGS[1]
+    wl = W.make_config(1, "cpu")
+    out, lse, dec = gpu_decode(wl.to("cuda"), num_splits=splits, fuse_merge=fuse)
+    ref_o, ref_l = oracle_full(wl)
+    assert_close(spec.kv, out, lse, ref_o, ref_l, what=f"cfg1 S={splits}")
+
+
+SMALL = [
+    # name, B, Hq, Hkv, D, ps, kv, q, lens
+    ("mha f16 d64", 2, 4, 4, 64, 16, "f16", "f16", [1, 200]),
+    ("gqa bf16 g4", 3, 16, 4, 128, 16, "bf16", "bf16", [64, 65, 1000]),
+    ("gqa bf16 g8 ps32", 2, 16, 2, 128, 32, "bf16", "bf16", [33, 777]),
+    ("gqa f16 g2 ps48", 2, 8, 4, 128, 48, "f16", "f16", [47, 500]),
+    ("gqa bf16 g16", 2, 32, 2, 128, 16, "bf16", "bf16", [100, 300]),
+    ("gqa bf16 g3", 2, 6, 2, 64, 64, "bf16", "bf16", [5, 129]),
+    ("fp8 bf16q g8 ps128", 3, 16, 2, 128, 128, "e4m3", "bf16", [16, 130, 1500]),
+    ("fp8 f16q g4 ps16", 2, 8, 2, 128, 16, "e4m3", "f16", [31, 400]),
+    ("fp8 bf16q d64 g1", 2, 2, 2, 64, 64, "e4m3", "bf16", [70, 9]),
+    ("fp8 bf16q g16", 1, 32, 2, 128, 128, "e4m3", "bf16", [700]),
+    ("empty and one token", 3, 8, 2, 128, 16, "bf16", "bf16", [0, 1, 17]),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_small_shapes(fdlib, case, splits):
+    spec = _spec(*case)
+    _run_and_check(spec, seed=7 + splits, num_splits=splits)
+
+
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("f16", "f16"), ("e4m3", "bf16")])
+def test_fp32_output(fdlib, kv, q):
+    spec = _spec("f32 out", 2, 8, 2, 128, 16, kv, q, [90, 333])
+    _run_and_check(spec, seed=3, out_dtype=torch.float32, num_splits=2)
+
+
+def test_config2_single_sequence_mha(fdlib):
+    wl = W.make_config(2, "cpu")
+    out, lse, dec = gpu_decode(wl.to("cuda"))
+    assert dec.plan.num_splits > 1
+    ref_o, ref_l = oracle_full(wl)
+    assert_close("f16", out, lse, ref_o, ref_l, "cfg2")
+
+
+def test_config4_long_context(fdlib):
+    wl = W.make_config(4, "cpu")
+    out, lse, dec = gpu_decode(wl.to("cuda"))
+    assert 16 <= dec.plan.num_splits <= 64
+    ref_o, ref_l = oracle_full(wl)
+    assert_close("bf16", out, lse, ref_o, ref_l, "cfg4")
+
+
+def _sample_pairs(wl, n, seed):
+    lens = wl.seq_lens.cpu().numpy()
+    B, Hq = wl.spec.B, wl.spec.Hq
+    rng = np.random.default_rng(seed)
+    bs = [int(np.argmax(lens)), int(np.argmin(lens)), 0, B - 1] + rng.integers(0, B, n).tolist()
+    return [(b, int(rng.integers(0, Hq))) for b in bs] + [(int(np.argmax(lens)), Hq - 1)]
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_batched_configs_sampled(fdlib, cfg):
+    wl = W.make_config(cfg, "cuda")
+    out, lse, dec = gpu_decode(wl)
+    wl_cpu = wl.to("cpu")
+    pairs = _sample_pairs(wl_cpu, 40, cfg)
+    ref_o, ref_l = oracle_pairs(wl_cpu, pairs)
+    idx_b = torch.tensor([p[0] for p in pairs])
+    idx_h = torch.tensor([p[1] for p in pairs])
+    o = out.cpu()[idx_b, idx_h]
+    l = lse.cpu()[idx_b, idx_h]
+    assert_close(wl.spec.kv, o, l, ref_o, ref_l, f"cfg{cfg} sampled")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_paged_equals_contiguous_bitexact(fdlib):
+    """Same tokens laid out under a random page permutation and under an
+    identity table give bit-identical GPU results for the same plan."""
+    spec = _spec("perm", 3, 16, 4, 128, 16, "bf16", "bf16", [100, 1000, 2500])
+    wl = W.make(spec, 11, "cpu")
+    ps = spec.page_size
+    lens = wl.seq_lens.tolist()
+    npg = [(L + ps - 1) // ps for L in lens]
+    total = sum(npg)
+    kc = torch.empty((total,) + tuple(wl.k_pages.shape[1:]), dtype=wl.k_pages.dtype)
+    vc = torch.empty_like(kc)
+    bt2 = torch.full_like(wl.block_table, -1)
+    cur = 0
+    for b, n in enumerate(npg):
+        for j in range(n):
+            src = int(wl.block_table[b, j])
+            kc[cur] = wl.k_pages[src]
+            vc[cur] = wl.v_pages[src]
+            bt2[b, j] = cur
+            cur += 1
+    wl2 = W.Workload(spec, wl.q, kc, vc, None, None, bt2, wl.seq_lens, total)
+    for splits in (1, 3):
+        o1, l1, _ = gpu_decode(wl.to("cuda"), num_splits=splits, num_sms=148)
+        o2, l2, _ = gpu_decode(wl2.to("cuda"), num_splits=splits, num_sms=148)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_workspace_counters_return_to_zero(fdlib):
+    wl = W.make_config(4, "cuda")
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu())
+    for _ in range(3):
+        dec(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    ctr = dec.workspace[dec.plan.ws_counters:].view(torch.int32)
+    assert int(ctr.abs().sum()) == 0
+    dec.check()
+
+
+def test_bad_page_is_flagged_not_faulted(fdlib):
+    spec = _spec("bad", 2, 8, 2, 128, 16, "bf16", "bf16", [100, 300])
+    wl = W.make(spec, 5, "cuda")
+    bt = wl.block_table.clone()
+    bt[1, 3] = -1
+    bt[0, 2] = wl.num_pages + 5
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, bt, wl.seq_lens.cpu())
+    dec(wl.q, wl.k_pages, wl.v_pages, bt, wl.seq_lens)
+    torch.cuda.synchronize()
+    word = int(dec.status.item())
+    assert word & _lib.FD_DEV_BAD_PAGE
+    with pytest.raises(fd.FdError) as ei:
+        dec.check()
+    assert ei.value.code == _lib.FD_ERR_BAD_PAGE
+    # the context is still usable and a clean call still matches the oracle
+    _run_and_check(spec, seed=5)
+
+
+def test_length_above_capacity_is_flagged(fdlib):
+    spec = _spec("cap", 1, 8, 2, 128, 16, "bf16", "bf16", [200], extra_blocks=20)
+    wl = W.make(spec, 6, "cuda")
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu())
+    longer = wl.seq_lens + dec.plan.capacity_tokens
+    dec(wl.q, wl.k_pages, wl.v_pages, wl.block_table, longer)
+    torch.cuda.synchronize()
+    assert int(dec.status.item()) & _lib.FD_DEV_CAPACITY
+    with pytest.raises(fd.FdError):
+        dec.check()
+
+
+def test_cuda_graph_replay_matches_eager(fdlib):
+    wl = W.make_config(2, "cuda")
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu())
+    out = torch.empty_like(wl.q)
+    lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            dec(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = out.clone(), lse.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dec(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens, out=out, lse=lse)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    dec.check()
+
+
+def test_plan_reused_while_lengths_grow(fdlib):
+    """A plan made with headroom serves later steps after appends (the
+    caller advances seq_lens, as the cookbook's decode loop does)."""
+    spec = _spec("grow", 2, 8, 2, 128, 16, "bf16", "bf16", [300, 47], extra_blocks=2)
+    wl = W.make(spec, 8, "cpu")
+    g = wl.to("cuda")
+    dec = fd.PagedDecoder.for_pools(g.q, g.k_pages, g.v_pages, g.block_table, wl.seq_lens,
+                                    max_seq_len=int(wl.seq_lens.max()) + 20)
+    lens = g.seq_lens.clone()
+    gen = torch.Generator().manual_seed(3)
+    for step in range(3):
+        kn = torch.randn((2, 2, 128), generator=gen).to(torch.bfloat16).cuda()
+        vn = torch.randn((2, 2, 128), generator=gen).to(torch.bfloat16).cuda()
+        fd.append_kv(torch.bfloat16, kn, vn, g.k_pages, g.v_pages, g.block_table, lens)
+        lens += 1
+        out, lse = dec(g.q, g.k_pages, g.v_pages, g.block_table, lens)
+        torch.cuda.synchronize()
+        dec.check()
+        cpu = W.Workload(spec, wl.q, g.k_pages.cpu(), g.v_pages.cpu(), None, None, wl.block_table, lens.cpu(),
+                         wl.num_pages)
+        ref_o, ref_l = oracle_full(cpu)
+        assert_close("bf16", out, lse, ref_o, ref_l, f"grow step {step}")

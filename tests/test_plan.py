@@ -1,0 +1,85 @@
+"""Host tests of the split-count planner (fd_plan): the pages' worked
+examples, their policy statements, and plan invariants."""
+import os
+
+import pytest
+import torch
+
+from split_kv_decode_paged_gb300 import _lib
+from split_kv_decode_paged_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name, key):
+    out = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#", 1)[0].split()
+        if line and line[0] == key:
+            out.append([int(x) for x in line[1:]])
+    return out
+
+
+def _prob(B, Hq, Hkv, L, D=128, ps=16, dt=torch.bfloat16, kv=None):
+    return _lib.make_problem(B, Hq, Hkv, D, ps, (L + ps - 1) // ps + 1, B * ((L + ps - 1) // ps + 1), dt,
+                             kv or dt)
+
+
+@pytest.mark.parametrize("row", _rows("cookbook_split_examples.txt", "example"))
+def test_cookbook_split_examples(fdlib, row):
+    sms, B, Hq, Hkv, L, margin, lo, hi = row
+    plan = _lib.fd_plan(_prob(B, Hq, Hkv, L), [L] * B, num_sms=sms, split_margin_pct=margin)
+    splits = (L + plan.chunk_tokens - 1) // plan.chunk_tokens
+    assert lo <= splits <= hi, (splits, plan.as_dict())
+
+
+@pytest.mark.parametrize("row", _rows("cookbook_split_examples.txt", "chunks"))
+def test_cookbook_split_ranges(fdlib, row):
+    L, S, chunk = row
+    plan = _lib.fd_plan(_prob(1, 8, 8, L), [L], num_sms=132, num_splits=S)
+    assert plan.chunk_tokens == chunk and plan.num_splits == S
+
+
+def test_short_sequences_are_not_split(fdlib):
+    # lpnh.cn "进阶突破": short sequences are not split, very long ones heavily.
+    for L in (1, 64, 300, 512):
+        plan = _lib.fd_plan(_prob(1, 32, 8, L), [L], num_sms=148)
+        assert plan.num_splits == 1
+    splits = []
+    for L in (4096, 16384, 131072):
+        plan = _lib.fd_plan(_prob(1, 32, 8, L), [L], num_sms=148)
+        splits.append((L + plan.chunk_tokens - 1) // plan.chunk_tokens)
+    assert splits[0] > 1 and splits[-1] >= splits[0]
+
+
+def test_long_context_config_split_range(fdlib):
+    # The 131072-token single request: roughly 16 to 64 splits on 148 SMs.
+    for sms in (148, 152):
+        plan = _lib.fd_plan(_prob(1, 32, 8, 131072, ps=64), [131072], num_sms=sms)
+        assert 16 <= plan.num_splits <= 64
+
+
+def test_full_batch_of_equal_lengths_is_not_split(fdlib):
+    # "Inference Cookbook" §6.3: no split once batch x heads fills the SMs.
+    plan = _lib.fd_plan(_prob(64, 32, 8, 4096), [4096] * 64, num_sms=148, split_margin_pct=18)
+    assert plan.num_splits == 1
+
+
+def test_plan_invariants(fdlib):
+    for cfg in (1, 2, 3, 4, 5):
+        spec = W.CONFIGS[cfg]
+        lens = W.draw_lengths(spec, torch.Generator().manual_seed(W.config_seed(cfg)))
+        mb = int((int(lens.max()) + spec.page_size - 1) // spec.page_size)
+        prob = _lib.make_problem(spec.B, spec.Hq, spec.Hkv, spec.D, spec.page_size, mb, spec.B * mb,
+                                 W._DT[spec.q], W._DT[spec.kv])
+        plan = _lib.fd_plan(prob, lens, num_sms=148)
+        assert plan.chunk_tokens % plan.tile_tokens == 0
+        assert plan.capacity_tokens >= int(lens.max())
+        assert 1 <= plan.num_splits <= 512 and plan.grid_ctas <= 148
+        assert plan.smem_bytes <= 232448 and 2 <= plan.stages <= 8
+        rows = spec.B * spec.Hq
+        assert plan.workspace_bytes >= (rows * plan.num_splits * (spec.D + 2) * 4 if plan.num_splits > 1 else 0)
+        # headroom for growth widens the capacity
+        plan2 = _lib.fd_plan(prob, lens, num_sms=148, max_seq_len=int(lens.max()) + 1000) \
+            if int(lens.max()) + 1000 <= spec.page_size * mb else plan
+        assert plan2.capacity_tokens >= plan.capacity_tokens
