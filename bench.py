@@ -1,0 +1,419 @@
+"""Benchmark: paged split-KV decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+One step = one fd_decode_paged call (split + merge) over one batch of the
+synthetic workload, inputs resident in HBM.  Every timed step is preceded by
+an L2 flush (a write of 2x the L2 size) outside the CUDA-event pair on the
+launching stream.  Prints ONE JSON line (rank 0).
+
+metric: achieved HBM GB/s of the decode call = algorithmic bytes (K+V of the
+live tokens, q, out, lse, live block-table entries, seq_lens, FP8 scales) /
+device time; us per call is reported beside it.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (seed
+offset by rank, no collective on the data path: weak scaling) and value =
+bytes of all ranks / max over ranks of the elapsed time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+HEADLINE_CONFIG = 3
+METRIC = "decode-attention achieved HBM GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "split_kv_decode_paged_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_tag):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"fd_split_kv_decode_kernel_{workload_tag}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(elapsed_s, bytes_done, group=None):
+    """Whole-job aggregation across ranks: total bytes and the max elapsed
+    time.  Works with any torch.distributed backend (gloo on CPU tensors in
+    the tests, NCCL on the GPU)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return elapsed_s, bytes_done
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend(group) == "nccl" else torch.device("cpu")
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(bytes_done)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), int(b.item())
+
+
+# ------------------------------------------------------------- GPU timing
+def time_decode(wl, steps, warmup, flush, stream=None, **plan_opts):
+    import split_kv_decode_paged_gb300 as fd
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu(), **plan_opts)
+    out = torch.empty_like(wl.q)
+    lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=wl.q.device)
+    args = (wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens)
+    kw = dict(k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse)
+    for _ in range(warmup):
+        flush.zero_()
+        dec(*args, **kw)
+    torch.cuda.synchronize()
+    dec.check()
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(st)
+        dec(*args, **kw)
+        ev[i][1].record(st)
+    torch.cuda.synchronize()
+    dec.check()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return ms, dec
+
+
+def time_warm_and_graph(wl, dec, iters=50):
+    """Warm-L2 and CUDA-graph-replay per-call times (labelled as such)."""
+    out = torch.empty_like(wl.q)
+    lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=wl.q.device)
+    args = (wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens)
+    kw = dict(k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            dec(*args, **kw)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(iters):
+            dec(*args, **kw)
+        b.record(s)
+    torch.cuda.synchronize()
+    warm = a.elapsed_time(b) / iters
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(10):
+            dec(*args, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters // 10):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    graph = a.elapsed_time(b) / (iters // 10 * 10)
+    dec.check()
+    return warm, graph
+
+
+def time_e2e(wl, dec, steps):
+    """End to end through the public API with host buffers: pinned H2D of the
+    step inputs (q, block table, seq_lens), the decode call, D2H of out and
+    lse, all inside the timed region.  The paged K/V cache is state that
+    lives in HBM across steps."""
+    q_h = wl.q.cpu().pin_memory()
+    bt_h = wl.block_table.cpu().pin_memory()
+    sl_h = wl.seq_lens.cpu().pin_memory()
+    q_d, bt_d, sl_d = torch.empty_like(wl.q), torch.empty_like(wl.block_table), torch.empty_like(wl.seq_lens)
+    out_d = torch.empty_like(wl.q)
+    lse_d = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=wl.q.device)
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    lse_h = torch.empty(lse_d.shape, dtype=torch.float32).pin_memory()
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        dec(q_d, wl.k_pages, wl.v_pages, bt_d, sl_d, k_scale=wl.k_scale, v_scale=wl.v_scale, out=out_d, lse=lse_d)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    dec.check()
+    return dt, h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_baseline(wl_cpu, target_s=12.0, seed=0):
+    import numpy as np
+    from oracle import oracle as orc
+    s = wl_cpu.spec
+    code = {torch.float16: orc.F16, torch.bfloat16: orc.BF16, torch.float8_e4m3fn: orc.E4M3}
+    p = orc.problem(s.B, s.Hq, s.Hkv, s.D, s.page_size, wl_cpu.max_blocks, wl_cpu.num_pages,
+                    code[wl_cpu.q.dtype], code[wl_cpu.k_pages.dtype])
+    lens = wl_cpu.seq_lens.numpy().astype(np.int64)
+    total_work = int(lens.sum()) * s.Hq
+    cores = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(seed)
+    order = [(int(b), int(h)) for b in rng.permutation(s.B) for h in rng.permutation(s.Hq)]
+    # calibrate on a small batch, then size the sample to ~target_s
+    done, work, elapsed = 0, 0, 0.0
+    n = max(cores, 8)
+    while done < len(order) and elapsed < target_s:
+        batch = order[done:done + n]
+        t0 = time.perf_counter()
+        orc.decode_paged_pairs(p, wl_cpu.q, wl_cpu.k_pages, wl_cpu.v_pages, wl_cpu.k_scale, wl_cpu.v_scale,
+                               wl_cpu.block_table, wl_cpu.seq_lens, batch, nthreads=cores)
+        elapsed += time.perf_counter() - t0
+        work += sum(int(lens[b]) for b, _ in batch)
+        done += len(batch)
+        rate = work / max(elapsed, 1e-9)
+        n = max(cores, int(rate * min(target_s - elapsed, target_s / 3) / max(1, lens.mean())))
+    us_per_call = elapsed / max(work, 1) * total_work * 1e6
+    from split_kv_decode_paged_gb300 import workloads as W
+    gbs = W.algorithmic_bytes(s, wl_cpu.seq_lens) / (us_per_call * 1e-6) / 1e9
+    return {"value": gbs, "unit": "GB/s", "us_per_call": us_per_call, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {s.B * s.Hq} (b, hq) pairs, {work} of {total_work} token-heads, "
+                      f"{elapsed:.1f} s fp64 on {cores} host threads, scaled to one call by token-heads"}
+
+
+# ------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=HEADLINE_CONFIG)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--all-configs", action="store_true", help="also report every workload (per_config)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--quick", action="store_true",
+                    help="only the timed decode calls (no warm-L2/graph/e2e extras, no CPU baseline)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from split_kv_decode_paged_gb300 import workloads as W
+    ws, rank, local = dist_env()
+    spec = W.CONFIGS[args.config]
+    tag = {1: "tiny_mha", 2: "single_seq_mha", 3: "gqa_batch", 4: "long_context", 5: "mixed_fp8"}[args.config]
+    config = {"workload": f"{spec.name} (config {args.config})", "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv,
+              "D": spec.D, "page_size": spec.page_size, "kv_dtype": spec.kv, "q_dtype": spec.q,
+              "lengths": list(spec.lens), "l2": "flushed before every timed call (2x L2 write)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = W.make_config(args.config, "cpu", seed=W.config_seed(args.config))
+        per, cb = [], None
+        per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+        for i in range(args.warmup + args.steps):
+            cb = cpu_baseline(wl, target_s=per_step, seed=i)
+            if i >= args.warmup:
+                per.append(cb["us_per_call"])
+        us = statistics.median(per)
+        bytes_call = W.algorithmic_bytes(spec, wl.seq_lens)
+        gbs = bytes_call / (us * 1e-6) / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "us_per_call": us,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+                                 "sample": f"each step: {cb['sample']}"},
+                "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from split_kv_decode_paged_gb300 import build as fd_build
+    if rank == 0 or ws == 1:
+        fd_build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    wl = W.make_config(args.config, dev, seed=W.config_seed(args.config) + 7919 * rank)
+    bytes_call = W.algorithmic_bytes(spec, wl.seq_lens.cpu())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=dev)
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(index=dev.index) as clk:
+        t0 = time.perf_counter()
+        ms, dec = time_decode(wl, args.steps, args.warmup, flush)
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    total_ms = sum(ms)
+    elapsed_s, bytes_all = aggregate(total_ms / 1e3, bytes_call * args.steps)
+    value = bytes_all / elapsed_s / 1e9
+    med = statistics.median(ms)
+    srt = sorted(ms)
+    peak, peak_kind = measured_peak()
+    achieved = bytes_call / (total_ms / args.steps * 1e-3) / 1e9
+    if args.quick:
+        warm_ms = graph_ms = float("nan")
+        e2e_s, h2d, d2h = float("nan"), 0, 0
+        args.no_cpu_baseline = True
+    else:
+        warm_ms, graph_ms = time_warm_and_graph(wl, dec)
+        e2e_s, h2d, d2h = time_e2e(wl, dec, max(10, args.steps // 2))
+    plan = dec.plan
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "us_per_call": total_ms / args.steps * 1e3,
+        "us_median": med * 1e3, "us_p10": srt[len(srt) // 10] * 1e3, "us_p90": srt[(len(srt) * 9) // 10] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3 (f16 MMA, fp32 accumulate)"}[spec.kv],
+        "data": "synthetic (seeded; see DESIGN.md input recipe)", "config": config,
+        "algorithmic_bytes_per_call": bytes_call,
+        "plan": {"num_splits": plan.num_splits, "chunk_tokens": plan.chunk_tokens, "grid_ctas": plan.grid_ctas,
+                 "stages": plan.stages, "work_items": plan.work_items_hint, "fuse_merge": plan.fuse_merge},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(tag),
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json burst copy)"},
+        "warm_l2_us_per_call": None if args.quick else warm_ms * 1e3,
+        "graph_replay_us_per_call": None if args.quick else graph_ms * 1e3,
+        "e2e": None if args.quick else {"value": bytes_call / e2e_s / 1e9, "unit": "GB/s",
+                                        "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
+                                        "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 if plan.fuse_merge or plan.num_splits == 1 else 2),
+        "clocks": clk.summary(), "wall_s_timed_region": wall,
+    }
+    if args.all_configs and rank == 0:
+        per = {}
+        for c in (1, 2, 3, 4, 5):
+            if c == args.config:
+                per[c] = {"us": total_ms / args.steps * 1e3, "gbs": achieved, "frac": achieved / peak}
+                continue
+            w2 = W.make_config(c, dev)
+            b2 = W.algorithmic_bytes(W.CONFIGS[c], w2.seq_lens.cpu())
+            ms2, d2 = time_decode(w2, 30, 3, flush)
+            t2 = sum(ms2) / len(ms2)
+            per[c] = {"us": t2 * 1e3, "gbs": b2 / (t2 * 1e-3) / 1e9, "frac": b2 / (t2 * 1e-3) / 1e9 / peak,
+                      "splits": d2.plan.num_splits, "chunk": d2.plan.chunk_tokens}
+            del w2, d2
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+    if rank == 0 and not args.no_cpu_baseline:
+        wl_cpu = wl.to("cpu")
+        line["cpu_baseline"] = cpu_baseline(wl_cpu, target_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
