@@ -47,10 +47,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+DECODE_KERNEL_FILES = ("decode_kernel.cuh", "decode_dispatch.cuh", "decode_f16.cu", "decode_bf16.cu",
+                       "decode_e4m3.cu", "ptx.cuh", "fd_internal.h")
+
+
 def kernel_source_hash():
+    """Hash of the sources that define the decode kernel (ties a committed
+    ncu traffic figure to the kernel it was measured on)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_decode_paged_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DECODE_KERNEL_FILES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -82,6 +88,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.first = 0
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -89,10 +96,14 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()  # start timing only once samples flow
+            while not self.lines and time.time() - t0 < 3.0:
+                time.sleep(0.01)
+            self.first = len(self.lines)
         except Exception:
             self.proc = None
         return self
@@ -287,7 +298,7 @@ def cpu_baseline(wl_cpu, target_s=12.0, seed=0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=HEADLINE_CONFIG)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])

@@ -476,6 +476,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const bool v0 = g < nloc, v1 = (g + 8) < nloc;
             float alpha[NT][2];
             uint32_t pb[NT][2];
+            uint32_t pl[NT][2];  // bf16 V: low parts of the weights (P = hi + lo)
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 const float s0 = v0 ? sacc[n][0] * sc : -INFINITY;
@@ -500,10 +501,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 uint32_t x0, x1;
                 float r0, r1, r2, r3;  // the rounded weights actually used
                 if constexpr (KV == KV_BF16) {
+                    // bf16 keeps 8 significant bits; the weights enter P.V as
+                    // hi + lo bf16 pairs (two MMAs on one V fragment), so the
+                    // product sees them to ~2^-17 relative.
                     x0 = pack_bf16x2(p0, p1);
                     x1 = pack_bf16x2(p2, p3);
-                    r0 = __uint_as_float(x0 << 16); r1 = __uint_as_float(x0 & 0xffff0000u);
-                    r2 = __uint_as_float(x1 << 16); r3 = __uint_as_float(x1 & 0xffff0000u);
+                    const float h0 = __uint_as_float(x0 << 16), h1 = __uint_as_float(x0 & 0xffff0000u);
+                    const float h2 = __uint_as_float(x1 << 16), h3 = __uint_as_float(x1 & 0xffff0000u);
+                    const uint32_t y0 = pack_bf16x2(p0 - h0, p1 - h1);
+                    const uint32_t y1 = pack_bf16x2(p2 - h2, p3 - h3);
+                    r0 = h0 + __uint_as_float(y0 << 16); r1 = h1 + __uint_as_float(y0 & 0xffff0000u);
+                    r2 = h2 + __uint_as_float(y1 << 16); r3 = h3 + __uint_as_float(y1 & 0xffff0000u);
+                    pl[n][0] = movmatrix_t(y0);
+                    pl[n][1] = movmatrix_t(y1);
                 } else {
                     x0 = pack_f16x2(p0, p1);
                     x1 = pack_f16x2(p2, p3);
@@ -543,10 +553,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23;
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        if constexpr (KV == KV_BF16)
+                        if constexpr (KV == KV_BF16) {
                             mma_bf16(o[mi][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
-                        else
+                            mma_bf16(o[mi][n], a0, a1, a2, a3, pl[n][0], pl[n][1]);
+                        } else {
                             mma_f16(o[mi][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
+                        }
                     }
                 }
             } else {

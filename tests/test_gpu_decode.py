@@ -55,9 +55,10 @@ SMALL = [
 
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 @pytest.mark.parametrize("splits", [0, 1, 3])
-def test_small_shapes(fdlib, case, splits):
+@pytest.mark.parametrize("out32", [False, True], ids=["out-native", "out-f32"])
+def test_small_shapes(fdlib, case, splits, out32):
     spec = _spec(*case)
-    _run_and_check(spec, seed=7 + splits, num_splits=splits)
+    _run_and_check(spec, seed=7 + splits, out_dtype=torch.float32 if out32 else None, num_splits=splits)
 
 
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("f16", "f16"), ("e4m3", "bf16")])
