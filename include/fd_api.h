@@ -189,6 +189,40 @@ fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void 
                        const float *v_scale, const int32_t *block_table,
                        const int32_t *seq_lens, int32_t *status_dev, void *stream);
 
+/* Size of the library-owned workspace used by fd_decode_paged_noalloc: 16 MiB
+ * per GPU that loads the library, held until the process exits. */
+#define FD_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* fd_decode_paged without a caller-provided workspace.  (The pages have no
+ * counterpart: this is a convenience of this library.)
+ *
+ * Who needs it: callers that cannot allocate device memory at the point of
+ * the call -- code hosted by an engine or plugin interface that owns every
+ * device allocation and hands out only input and output pointers, real-time
+ * loops that must not take cudaMalloc's device-wide synchronisation, and
+ * plain C callers that have no device allocator at hand.
+ *
+ * The workspace is a fixed buffer of FD_NOALLOC_SCRATCH_BYTES inside libfd,
+ * one per device.  Arguments are those of fd_decode_paged minus the
+ * workspace.  The caller still owns q, the pools, the block table, seq_lens,
+ * out, lse and status_dev.
+ *  - Returns FD_ERR_WORKSPACE_TOO_SMALL, with nothing launched, when
+ *    plan->workspace_bytes exceeds FD_NOALLOC_SCRATCH_BYTES (plan with fewer
+ *    splits, or call fd_decode_paged with a workspace of your own).
+ *  - The first call on each device looks up the device address of that
+ *    device's buffer; make that first call before any stream capture.
+ *  - Every call on a device uses the same buffer, which keeps what the last
+ *    call left in it; each call clears the buffer's counters with an
+ *    asynchronous memset on `stream` before the decode launch.  Calls whose
+ *    GPU work overlaps (other streams, other threads) race on the buffer and
+ *    give wrong results: order them, e.g. on one stream.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+fd_status fd_decode_paged_noalloc(const fd_plan_t *plan, const void *q, const void *k_pages,
+                                  const void *v_pages, const float *k_scale,
+                                  const float *v_scale, const int32_t *block_table,
+                                  const int32_t *seq_lens, void *out, float *lse,
+                                  int32_t *status_dev, void *stream);
+
 /* Map a device status word to a status code (FD_OK when zero). */
 fd_status fd_status_from_device(int32_t status_word);
 

@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fd_api.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "merge.cu", "append.cu"]
+SOURCES = ["fd_api.cu", "decode_f16.cu", "decode_bf16.cu", "decode_e4m3.cu", "merge.cu", "append.cu",
+           "noalloc.cu"]
 
 
 def nvcc() -> str:

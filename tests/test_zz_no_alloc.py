@@ -1,0 +1,90 @@
+"""fd_decode_paged_noalloc: the decode entry point that takes no workspace.
+
+It is for callers that cannot allocate device memory where they call the
+library (an engine or plugin interface that owns all device allocations,
+loops that must not take cudaMalloc's synchronisation, C callers without an
+allocator).  Its workspace is a fixed buffer inside libfd.  These tests call
+it through the C ABI, twice in a row on the same buffer, and compare with the
+workspace-taking fd_decode_paged on the same plan and inputs, within the
+parity tolerance the other tests use.  This file is collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import split_kv_decode_paged_gb300 as fd
+from split_kv_decode_paged_gb300 import _lib
+from split_kv_decode_paged_gb300 import workloads as W
+from tests.gpu_helpers import TOL_OUT, TOL_LSE, half_ulp
+
+pytestmark = pytest.mark.gpu
+
+NOALLOC_MAX = 16 * 1024 * 1024  # FD_NOALLOC_SCRATCH_BYTES in include/fd_api.h
+
+
+def _noalloc_fn(lib):
+    f = lib.fd_decode_paged_noalloc
+    P = ctypes.c_void_p
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(_lib.FdPlan), P, P, P, P, P, P, P, P, P, P, P]
+    return f
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _close(kv, got, ref_out, got_lse, ref_lse):
+    a = got.double().cpu().numpy()
+    b = ref_out.double().cpu().numpy()
+    assert np.isfinite(a).all()
+    assert (np.abs(a - b) <= TOL_OUT[kv] + half_ulp(b, got.dtype)).all()
+    la, lb = got_lse.double().cpu().numpy(), ref_lse.double().cpu().numpy()
+    same_inf = np.isneginf(la) & np.isneginf(lb)
+    assert (np.abs(np.where(same_inf, 0.0, la - np.where(same_inf, 0.0, lb))) <= TOL_LSE[kv]).all()
+
+
+CASES = [
+    ("single-sequence MHA, split", W.CONFIGS[2], {}),
+    ("GQA bf16, forced 3 splits, ragged", W.Spec("gqa", B=3, Hq=16, Hkv=4, D=128, page_size=16, kv="bf16",
+                                                 q="bf16", lens=("list", [0, 700, 2100])), {"num_splits": 3}),
+    ("FP8 pages, 2 splits", W.Spec("fp8", B=2, Hq=16, Hkv=2, D=128, page_size=128, kv="e4m3", q="bf16",
+                                   lens=("list", [130, 1500])), {"num_splits": 2}),
+]
+
+
+@pytest.mark.parametrize("name,spec,opts", CASES, ids=[c[0] for c in CASES])
+def test_noalloc_matches_workspace_entry_point(fdlib, name, spec, opts):
+    wl = W.make(spec, 21, "cuda")
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu(), **opts)
+    assert dec.plan.workspace_bytes <= NOALLOC_MAX
+    ref_out, ref_lse = dec(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens, wl.k_scale, wl.v_scale)
+    torch.cuda.synchronize()
+    dec.check()
+
+    f = _noalloc_fn(fdlib)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):  # the second call reuses the buffer the first one left behind
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        rc = f(ctypes.byref(dec.plan), _p(wl.q), _p(wl.k_pages), _p(wl.v_pages), _p(wl.k_scale),
+               _p(wl.v_scale), _p(wl.block_table), _p(wl.seq_lens), _p(out), _p(lse), _p(status), stream)
+        assert rc == _lib.FD_OK, _lib.fd_status_string(rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        _close(spec.kv, out, ref_out, lse, ref_lse)
+
+
+def test_noalloc_rejects_plans_beyond_its_buffer(fdlib):
+    # 256 sequences x 64 heads of 32768-token capacity in 64 splits need far
+    # more partial-state room than the built-in buffer holds.
+    prob = _lib.make_problem(256, 64, 8, 128, 128, 256, 40000, torch.bfloat16, torch.float8_e4m3fn)
+    plan = _lib.fd_plan(prob, [32768] * 256, num_splits=64)
+    assert plan.workspace_bytes > NOALLOC_MAX
+    f = _noalloc_fn(fdlib)
+    fake = ctypes.c_void_p(1 << 20)  # never touched: the size check comes first
+    rc = f(ctypes.byref(plan), fake, fake, fake, fake, fake, fake, fake, fake, None, None, None)
+    assert rc == _lib.FD_ERR_WORKSPACE_TOO_SMALL
