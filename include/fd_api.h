@@ -100,6 +100,7 @@ typedef struct {
                            estimated time is within this many percent of the
                            best; 18 reproduces the cookbook's "smallest split
                            count reaching 85% of the best efficiency" [P3 §6.3] */
+    int tile_tokens;    /* 0 = default (128); 64 or 128 tokens per pipeline stage */
 } fd_plan_options;
 
 /* A plan: plain data in host memory, owned by the caller, reusable for any

@@ -4,18 +4,42 @@
 
 namespace fd {
 
+// (consumer warps, sub-tiles per warp) pairs built for each storage kind:
+// 16-bit K/V: (4,1) = 64-token stages, (4,2) = 128-token stages;
+// E4M3 K/V:   (4,1) = 64-token stages, (8,1) = 128-token stages.
+template <int KV, int D, int NT, bool QBF16>
+cudaError_t launch_decode_d(const KernelShape &ks, const DecodeParams &dp, const CUtensorMap &tmk,
+                            const CUtensorMap &tmv, int grid, size_t smem, cudaStream_t stream) {
+    if (ks.consumer_warps == 4 && ks.subtiles == 1)
+        return launch_decode_t<KV, D, NT, 4, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);
+    if constexpr (KV == KV_E4M3) {
+        if (ks.consumer_warps == 8 && ks.subtiles == 1)
+            return launch_decode_t<KV, D, NT, 8, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);
+    } else {
+        if (ks.consumer_warps == 4 && ks.subtiles == 2)
+            return launch_decode_t<KV, D, NT, 4, 2, QBF16>(dp, tmk, tmv, grid, smem, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int KV, int D, int NT, bool QBF16>
+size_t decode_smem_d(const KernelShape &ks, int stages, int B) {
+    if (ks.consumer_warps == 4 && ks.subtiles == 1) return decode_smem_for<KV, D, NT, 4, 1, QBF16>(stages, B);
+    if (ks.consumer_warps == 8) return decode_smem_for<KV, D, NT, 8, 1, QBF16>(stages, B);
+    return decode_smem_for<KV, D, NT, 4, 2, QBF16>(stages, B);
+}
+
 template <int KV, bool QBF16>
 cudaError_t launch_decode_kind(const fd_problem &p, const KernelShape &ks, const DecodeParams &dp,
                                const CUtensorMap &tmk, const CUtensorMap &tmv, int grid, size_t smem,
                                cudaStream_t stream) {
-    if (ks.consumer_warps != 4) return cudaErrorInvalidValue;
     if (p.D == 128) {
-        if (ks.nt == 1) return launch_decode_t<KV, 128, 1, 4, QBF16>(dp, tmk, tmv, grid, smem, stream);
-        return launch_decode_t<KV, 128, 2, 4, QBF16>(dp, tmk, tmv, grid, smem, stream);
+        if (ks.nt == 1) return launch_decode_d<KV, 128, 1, QBF16>(ks, dp, tmk, tmv, grid, smem, stream);
+        return launch_decode_d<KV, 128, 2, QBF16>(ks, dp, tmk, tmv, grid, smem, stream);
     }
     if (p.D == 64) {
-        if (ks.nt == 1) return launch_decode_t<KV, 64, 1, 4, QBF16>(dp, tmk, tmv, grid, smem, stream);
-        return launch_decode_t<KV, 64, 2, 4, QBF16>(dp, tmk, tmv, grid, smem, stream);
+        if (ks.nt == 1) return launch_decode_d<KV, 64, 1, QBF16>(ks, dp, tmk, tmv, grid, smem, stream);
+        return launch_decode_d<KV, 64, 2, QBF16>(ks, dp, tmk, tmv, grid, smem, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -23,10 +47,10 @@ cudaError_t launch_decode_kind(const fd_problem &p, const KernelShape &ks, const
 template <int KV, bool QBF16>
 size_t decode_smem_kind(const fd_problem &p, const KernelShape &ks, int stages) {
     if (p.D == 128)
-        return ks.nt == 1 ? decode_smem_for<KV, 128, 1, 4, QBF16>(stages, p.B)
-                          : decode_smem_for<KV, 128, 2, 4, QBF16>(stages, p.B);
-    return ks.nt == 1 ? decode_smem_for<KV, 64, 1, 4, QBF16>(stages, p.B)
-                      : decode_smem_for<KV, 64, 2, 4, QBF16>(stages, p.B);
+        return ks.nt == 1 ? decode_smem_d<KV, 128, 1, QBF16>(ks, stages, p.B)
+                          : decode_smem_d<KV, 128, 2, QBF16>(ks, stages, p.B);
+    return ks.nt == 1 ? decode_smem_d<KV, 64, 1, QBF16>(ks, stages, p.B)
+                      : decode_smem_d<KV, 64, 2, QBF16>(ks, stages, p.B);
 }
 
 }  // namespace fd

@@ -51,13 +51,13 @@ struct StageMeta {
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int KV, int D, int NT, int NC>
+template <int KV, int D, int NT, int NC, int SUBT>
 struct DecodeShape {
     static constexpr int E = (KV == KV_E4M3) ? 1 : 2;  // K/V bytes per element
     static constexpr int RB = D * E;                   // bytes per K/V row
     static constexpr int SUBROW = RB > 128 ? 128 : RB; // swizzle span (bytes)
     static constexpr int NHALF = RB / SUBROW;          // sub-row regions per row
-    static constexpr int TILE = NC * kTokensPerWarp;   // tokens per stage
+    static constexpr int TILE = NC * SUBT * kTokensPerWarp;  // tokens per stage
     static constexpr int QROWS = 8 * NT;               // padded query rows
     static constexpr int KV_REGION = TILE * RB;
     static constexpr int Q_REGION = align_up(QROWS * D * 2, 1024);
@@ -138,11 +138,11 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int nsplit, f
     }
 }
 
-template <int KV, int D, int NT, int NC, bool QBF16>
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     fd_split_kv_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmv) {
-    using Sh = DecodeShape<KV, D, NT, NC>;
+    using Sh = DecodeShape<KV, D, NT, NC, SUBT>;
     constexpr int TILE = Sh::TILE, E = Sh::E, SUBROW = Sh::SUBROW, NHALF = Sh::NHALF;
     constexpr int QROWS = Sh::QROWS, SS = Sh::SS;
     constexpr bool FP8 = (KV == KV_E4M3);
@@ -265,8 +265,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 }
                 const int src_lane = (kb + (lane < BPT ? lane : 0)) & 31;
                 const int pg = __shfl_sync(0xffffffffu, pg_cur, src_lane);
-                const float ksc = __shfl_sync(0xffffffffu, ks_cur, src_lane);
-                const float vsc = __shfl_sync(0xffffffffu, vs_cur, src_lane);
+                float ksc = 1.f, vsc = 1.f;
+                if constexpr (FP8) {
+                    ksc = __shfl_sync(0xffffffffu, ks_cur, src_lane);
+                    vsc = __shfl_sync(0xffffffffu, vs_cur, src_lane);
+                }
                 const bool live = lane < BPT && (kb + lane) < nbox;
                 const bool good = live && pg >= 0 && pg < p.num_pages;
                 if (live && !good) flag_status(p.status, FD_DEV_BAD_PAGE);
@@ -288,9 +291,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     m->flags = (j == 0 ? kFlagFirst : 0) | (j == ntiles - 1 ? kFlagLast : 0);
                     m->nsplit = nsplit;
                 }
-                if (lane < BPT) {
-                    m->kscale[lane] = ksc;
-                    m->vscale[lane] = vsc;
+                if constexpr (FP8) {
+                    if (lane < BPT) {
+                        m->kscale[lane] = ksc;
+                        m->vscale[lane] = vsc;
+                    }
                 }
                 __syncwarp();
                 const uint32_t fb = smem_u32(&full_bar[st]);
@@ -303,14 +308,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     bulk_load(smem_u32(sb + 2 * Sh::KV_REGION), qsrc, (uint32_t)(p.G * D * 2), fb);
                 }
                 if (good) {
+                    // One box = boxr token rows x the whole D of one KV head,
+                    // stored as NHALF swizzled regions of boxr x SUBROW bytes.
                     const int tok = (box0 + kb + lane) * boxr;
                     const int slot = tok % ps;
-#pragma unroll
-                    for (int h = 0; h < NHALF; ++h) {
-                        const uint32_t off = (uint32_t)(h * TILE * SUBROW + lane * boxr * SUBROW);
-                        tma_load_4d(smem_u32(sb + off), &tmk, fb, h * (SUBROW / E), kvh, slot, pg);
-                        tma_load_4d(smem_u32(sb + Sh::KV_REGION + off), &tmv, fb, h * (SUBROW / E), kvh, slot, pg);
-                    }
+                    const uint32_t off = (uint32_t)(lane * NHALF * boxr * SUBROW);
+                    tma_load_5d(smem_u32(sb + off), &tmk, fb, 0, slot, 0, kvh, pg);
+                    tma_load_5d(smem_u32(sb + Sh::KV_REGION + off), &tmv, fb, 0, slot, 0, kvh, pg);
                 }
                 ++n_issued;
                 if (++st == NST) { st = 0; ph ^= 1u; }
@@ -420,10 +424,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
         }
 
-        const int nloc = max(0, min(kTokensPerWarp, nvalid - warp * kTokensPerWarp));
+#pragma unroll 1
+        for (int sub = 0; sub < SUBT; ++sub) {
+        // This warp's 16 tokens: tile rows r0 .. r0+15, inside box r0 / boxr
+        // (boxes hold NHALF swizzled regions of boxr rows x SUBROW bytes).
+        const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+        const int nloc = max(0, min(kTokensPerWarp, nvalid - r0));
         if (nloc > 0) {
-            const int row_a = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;  // QK: ldmatrix rows
-            const int row_t = warp * 16 + (lane & 7) + (lane >> 4) * 8;        // PV (f16/bf16): .trans rows
+            const int rib = r0 % p.boxr;  // first row inside the box (multiple of 16)
+            const uint32_t hstride = (uint32_t)(p.boxr * SUBROW);
+            const uint32_t box_off = (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
+            const uint32_t kbox = kbase + box_off, vbox = vbase + box_off;
+            const int row_a = rib + (lane & 7) + ((lane >> 3) & 1) * 8;  // QK: ldmatrix rows
+            const int row_t = rib + (lane & 7) + (lane >> 4) * 8;        // PV (f16/bf16): .trans rows
             // ---------------------------------------------------------- S = K Q^T
             float sacc[NT][4];
 #pragma unroll
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const int h = byte / SUBROW;
                     const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_a, chunk), a0, a1, a2, a3);
+                    ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), a0, a1, a2, a3);
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         if constexpr (KV == KV_BF16)
@@ -452,16 +465,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const int byte = jg * 32;
                     const int h = byte / SUBROW;
                     const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_a, chunk), r0, r1, r2, r3);
-                    const uint32_t a00 = e4m3x2_to_f16x2((uint16_t)(r0 & 0xffff));
-                    const uint32_t a01 = e4m3x2_to_f16x2((uint16_t)(r1 & 0xffff));
-                    const uint32_t a02 = e4m3x2_to_f16x2((uint16_t)(r0 >> 16));
-                    const uint32_t a03 = e4m3x2_to_f16x2((uint16_t)(r1 >> 16));
-                    const uint32_t a10 = e4m3x2_to_f16x2((uint16_t)(r2 & 0xffff));
-                    const uint32_t a11 = e4m3x2_to_f16x2((uint16_t)(r3 & 0xffff));
-                    const uint32_t a12 = e4m3x2_to_f16x2((uint16_t)(r2 >> 16));
-                    const uint32_t a13 = e4m3x2_to_f16x2((uint16_t)(r3 >> 16));
+                    uint32_t q0, q1, q2, q3;
+                    ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
+                    const uint32_t a00 = e4m3x2_to_f16x2((uint16_t)(q0 & 0xffff));
+                    const uint32_t a01 = e4m3x2_to_f16x2((uint16_t)(q1 & 0xffff));
+                    const uint32_t a02 = e4m3x2_to_f16x2((uint16_t)(q0 >> 16));
+                    const uint32_t a03 = e4m3x2_to_f16x2((uint16_t)(q1 >> 16));
+                    const uint32_t a10 = e4m3x2_to_f16x2((uint16_t)(q2 & 0xffff));
+                    const uint32_t a11 = e4m3x2_to_f16x2((uint16_t)(q3 & 0xffff));
+                    const uint32_t a12 = e4m3x2_to_f16x2((uint16_t)(q2 >> 16));
+                    const uint32_t a13 = e4m3x2_to_f16x2((uint16_t)(q3 >> 16));
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         mma_f16(sacc[n], a00, a01, a02, a03, qf[2 * jg][n][0], qf[2 * jg][n][1]);
@@ -472,7 +485,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 
             // ------------------------------------------------- online softmax (exp2)
             float sc = scale_log2;
-            if constexpr (FP8) sc *= mt.kscale[(warp * kTokensPerWarp) / p.boxr];
+            if constexpr (FP8) sc *= mt.kscale[r0 / p.boxr];
             const bool v0 = g < nloc, v1 = (g + 8) < nloc;
             float alpha[NT][2];
             uint32_t pb[NT][2];
@@ -499,7 +512,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 const float p2 = (mn0 == -INFINITY) ? 0.f : ex2(s2 - mn0);
                 const float p3 = (mn1 == -INFINITY) ? 0.f : ex2(s3 - mn1);
                 uint32_t x0, x1;
-                float r0, r1, r2, r3;  // the rounded weights actually used
+                float wr0, wr1, wr2, wr3;  // the rounded weights actually used
                 if constexpr (KV == KV_BF16) {
                     // bf16 keeps 8 significant bits; the weights enter P.V as
                     // hi + lo bf16 pairs (two MMAs on one V fragment), so the
@@ -510,8 +523,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const float h2 = __uint_as_float(x1 << 16), h3 = __uint_as_float(x1 & 0xffff0000u);
                     const uint32_t y0 = pack_bf16x2(p0 - h0, p1 - h1);
                     const uint32_t y1 = pack_bf16x2(p2 - h2, p3 - h3);
-                    r0 = h0 + __uint_as_float(y0 << 16); r1 = h1 + __uint_as_float(y0 & 0xffff0000u);
-                    r2 = h2 + __uint_as_float(y1 << 16); r3 = h3 + __uint_as_float(y1 & 0xffff0000u);
+                    wr0 = h0 + __uint_as_float(y0 << 16); wr1 = h1 + __uint_as_float(y0 & 0xffff0000u);
+                    wr2 = h2 + __uint_as_float(y1 << 16); wr3 = h3 + __uint_as_float(y1 & 0xffff0000u);
                     pl[n][0] = movmatrix_t(y0);
                     pl[n][1] = movmatrix_t(y1);
                 } else {
@@ -519,10 +532,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     x1 = pack_f16x2(p2, p3);
                     const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&x0));
                     const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&x1));
-                    r0 = f0.x; r1 = f0.y; r2 = f1.x; r3 = f1.y;
+                    wr0 = f0.x; wr1 = f0.y; wr2 = f1.x; wr3 = f1.y;
                 }
-                lrow[n][0] = lrow[n][0] * alpha[n][0] + (r0 + r2);
-                lrow[n][1] = lrow[n][1] * alpha[n][1] + (r1 + r3);
+                lrow[n][0] = lrow[n][0] * alpha[n][0] + (wr0 + wr2);
+                lrow[n][1] = lrow[n][1] * alpha[n][1] + (wr1 + wr3);
                 pb[n][0] = movmatrix_t(x0);
                 pb[n][1] = movmatrix_t(x1);
             }
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const int h = byte / SUBROW;
                     const int chunk = (byte % SUBROW) / 16 + ((lane >> 3) & 1);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_t, chunk), a0, a1, a2, a3);
+                    ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_t, chunk), a0, a1, a2, a3);
                     a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23;
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
@@ -562,16 +575,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     }
                 }
             } else {
-                const float vsc = mt.vscale[(warp * kTokensPerWarp) / p.boxr];
+                const float vsc = mt.vscale[r0 / p.boxr];
 #pragma unroll
                 for (int jg = 0; jg < D / 32; ++jg) {
                     const int byte = jg * 32;
                     const int h = byte / SUBROW;
                     const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vbase + (uint32_t)(h * TILE * SUBROW) + swz<SUBROW>(row_a, chunk), r0, r1, r2, r3);
-                    const uint32_t t0 = __byte_perm(r0, 0, 0x3120), t1 = __byte_perm(r1, 0, 0x3120);
-                    const uint32_t t2 = __byte_perm(r2, 0, 0x3120), t3 = __byte_perm(r3, 0, 0x3120);
+                    uint32_t q0, q1, q2, q3;
+                    ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
+                    const uint32_t t0 = __byte_perm(q0, 0, 0x3120), t1 = __byte_perm(q1, 0, 0x3120);
+                    const uint32_t t2 = __byte_perm(q2, 0, 0x3120), t3 = __byte_perm(q3, 0, 0x3120);
                     uint32_t A[2][4];
                     A[0][0] = e4m3x2_to_f16x2((uint16_t)(t0 & 0xffff)) & msk01;
                     A[0][1] = e4m3x2_to_f16x2((uint16_t)(t0 >> 16)) & msk01;
@@ -596,6 +609,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 }
             }
         }
+        }  // sub-tiles
         // Release the stage (all reads of it are done).
         const int m_kvh = mt.kvh, m_s = mt.s, m_nsplit = mt.nsplit;
         __syncwarp();
@@ -686,9 +700,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     }
 }
 
-template <int KV, int D, int NT, int NC, bool QBF16>
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
 size_t decode_smem_for(int stages, int B) {
-    using Sh = DecodeShape<KV, D, NT, NC>;
+    using Sh = DecodeShape<KV, D, NT, NC, SUBT>;
     size_t n = 1024;  // alignment slack
     n += (size_t)stages * Sh::STAGE;
     n += align_up(Sh::SCRATCH, 128);
@@ -698,13 +712,13 @@ size_t decode_smem_for(int stages, int B) {
     return n;
 }
 
-template <int KV, int D, int NT, int NC, bool QBF16>
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
 cudaError_t launch_decode_t(const DecodeParams &dp, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                             size_t smem, cudaStream_t stream) {
-    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, QBF16>;
+    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, DecodeShape<KV, D, NT, NC>::THREADS, smem, stream>>>(dp, tmk, tmv);
+    kern<<<grid, DecodeShape<KV, D, NT, NC, SUBT>::THREADS, smem, stream>>>(dp, tmk, tmv);
     return cudaGetLastError();
 }
 

@@ -23,10 +23,20 @@ size_t decode_smem_f16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
 
-KernelShape kernel_shape(const fd_problem &p) {
+KernelShape kernel_shape(const fd_problem &p, int tile_tokens) {
     KernelShape ks;
-    ks.consumer_warps = 4;
-    ks.tile = ks.consumer_warps * kTokensPerWarp;
+    const int tile = tile_tokens == 64 ? 64 : 128;
+    if (tile == 64) {
+        ks.consumer_warps = 4;
+        ks.subtiles = 1;
+    } else if (p.kv_dtype == FD_E4M3) {
+        ks.consumer_warps = 8;  // E4M3 needs more consumer issue per byte
+        ks.subtiles = 1;
+    } else {
+        ks.consumer_warps = 4;
+        ks.subtiles = 2;
+    }
+    ks.tile = ks.consumer_warps * ks.subtiles * kTokensPerWarp;
     ks.nt = (p.Hq / p.Hkv) <= 8 ? 1 : 2;
     return ks;
 }
@@ -197,21 +207,26 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// K or V pool viewed as (D, Hkv, page_size, num_pages); one box = `boxr`
-// token rows x one swizzle span of D for a single KV head.
+// K or V pool viewed as 5-D (d within a swizzle span, slot, span index,
+// kvh, page): one box = `boxr` token rows x all of D for one KV head, landing
+// in shared memory as [span][row][span bytes] so each span is one swizzled
+// region (a span is 128 bytes, or the whole row when the row is shorter).
 bool encode_pool_map(CUtensorMap *map, const void *pool, const fd_problem &p, int boxr) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int e = elem_bytes(p.kv_dtype);
     const int rb = p.D * e;
     const int span = rb > 128 ? 128 : rb;
-    cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.Hkv, (cuuint64_t)p.page_size, (cuuint64_t)p.num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)rb, (cuuint64_t)rb * p.Hkv, (cuuint64_t)rb * p.Hkv * p.page_size};
-    cuuint32_t box[4] = {(cuuint32_t)(span / e), 1u, (cuuint32_t)boxr, 1u};
-    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const int nspan = rb / span;
+    cuuint64_t dims[5] = {(cuuint64_t)(span / e), (cuuint64_t)p.page_size, (cuuint64_t)nspan, (cuuint64_t)p.Hkv,
+                          (cuuint64_t)p.num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)rb * p.Hkv, (cuuint64_t)span, (cuuint64_t)rb,
+                             (cuuint64_t)rb * p.Hkv * p.page_size};
+    cuuint32_t box[5] = {(cuuint32_t)(span / e), (cuuint32_t)boxr, (cuuint32_t)nspan, 1u, 1u};
+    cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
     const CUtensorMapDataType dt = e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
     const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUresult r = fn(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+    CUresult r = fn(map, dt, 5, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -248,10 +263,11 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (!plan || !seq_lens_host) return FD_ERR_INVALID_ARG;
     fd_status st = validate_problem(problem);
     if (st != FD_OK) return st;
-    fd_plan_options opt = {0, 0, 1, 0, 0, 0};
+    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0};
     if (options) opt = *options;
     if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 ||
-        opt.split_margin_pct < 0 || opt.split_margin_pct > 100)
+        opt.split_margin_pct < 0 || opt.split_margin_pct > 100 ||
+        (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128))
         return FD_ERR_INVALID_ARG;
     const double margin = (opt.split_margin_pct > 0 ? opt.split_margin_pct : kDefaultSplitMarginPct) / 100.0;
     const fd_problem &p = *problem;
@@ -276,7 +292,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         if (st != FD_OK) return st;
         sms = di.sms;
     }
-    const KernelShape ks = kernel_shape(p);
+    const KernelShape ks = kernel_shape(p, opt.tile_tokens);
     const int tile = ks.tile;
     const int ctas_per_sm = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
     const int P = sms * ctas_per_sm;
@@ -349,7 +365,7 @@ fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pa
         (v_scale && !aligned(v_scale, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return FD_ERR_INVALID_ARG;
     if (workspace_bytes < plan->workspace_bytes) return FD_ERR_WORKSPACE_TOO_SMALL;
-    const KernelShape ks = kernel_shape(p);
+    const KernelShape ks = kernel_shape(p, plan->tile_tokens);
     if (plan->tile_tokens != ks.tile || plan->chunk_tokens < ks.tile || plan->chunk_tokens % ks.tile != 0 ||
         plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->stages < kMinStages ||
         plan->stages > kMaxStages || plan->grid_ctas < 1)

@@ -14,7 +14,7 @@ namespace fd {
 // pipeline tile (tokens per stage) that follows from them.
 constexpr int kTokensPerWarp = 16;
 constexpr int kMaxConsumerWarps = 8;
-constexpr int kMaxBoxesPerTile = 8;
+constexpr int kMaxBoxesPerTile = 8;  // tile / gcd(page_size, tile) <= 128 / 16
 constexpr int kMaxSplits = 512;      // partial slots per (b, hq)
 constexpr int kMaxBatch = 8192;
 constexpr int kMinChunkTokens = 256; // below this a sequence is not split
@@ -72,11 +72,13 @@ struct AppendParams {
 // Kernel configuration chosen at plan time.
 struct KernelShape {
     int consumer_warps;  // 4 or 8
-    int tile;            // consumer_warps * kTokensPerWarp
+    int subtiles;        // 16-token sub-tiles per consumer warp per stage: 1 or 2
+    int tile;            // tokens per stage = consumer_warps * subtiles * 16
     int nt;              // 8-wide head tiles: 1 (G <= 8) or 2 (G <= 16)
 };
 
-KernelShape kernel_shape(const fd_problem &p);
+// tile_tokens: 64 or 128 (0 = default for the K/V type).
+KernelShape kernel_shape(const fd_problem &p, int tile_tokens);
 size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages);
 int decode_max_stages(const fd_problem &p, const KernelShape &ks);
 
