@@ -65,7 +65,7 @@ struct DecodeShape {
     static constexpr int SS = D + 4;                   // scratch row stride (floats)
     // Per-warp O rows; reused for the merge weights (QROWS x kMaxSplits).
     static constexpr int SCR_O = (NC * QROWS * SS > QROWS * kMaxSplits) ? NC * QROWS * SS : QROWS * kMaxSplits;
-    static constexpr int SCRATCH = SCR_O * 4 + 2 * NC * QROWS * 4 + 16;
+    static constexpr int SCRATCH = SCR_O * 4 + 2 * NC * QROWS * 4 + 2 * QROWS * 4 + 16;
     static constexpr int THREADS = (NC + 1) * 32;
     static_assert(D == 64 || D == 128, "D");
     static_assert(SUBROW == 128 || SUBROW == 64, "swizzle span");
@@ -87,6 +87,24 @@ __device__ __forceinline__ void flag_status(int *status, int bit) {
 template <typename T>
 __device__ __forceinline__ T ldcg(const T *p) {
     return __ldcg(p);
+}
+
+// Four consecutive outputs (idx a multiple of 4).
+__device__ __forceinline__ void store_out4(void *out, size_t idx, float a, float b, float c, float d,
+                                           int out_dtype) {
+    if (out_dtype == FD_BF16) {
+        uint2 v;
+        v.x = pack_bf16x2(a, b);
+        v.y = pack_bf16x2(c, d);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + idx) = v;
+    } else if (out_dtype == FD_F16) {
+        uint2 v;
+        v.x = pack_f16x2(a, b);
+        v.y = pack_f16x2(c, d);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(out) + idx) = v;
+    } else {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + idx) = make_float4(a, b, c, d);
+    }
 }
 
 __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int out_dtype) {
@@ -154,7 +172,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     float *scratch = reinterpret_cast<float *>(stages + (size_t)NST * Sh::STAGE);
     float *scr_m = scratch + Sh::SCR_O;
     float *scr_l = scr_m + NC * QROWS;
-    int *scr_flag = reinterpret_cast<int *>(scr_l + NC * QROWS);
+    float *scr_inv = scr_l + NC * QROWS;   // per head: 1 / combined denominator
+    float *scr_lse = scr_inv + QROWS;      // per head: combined max (log2 units)
+    int *scr_flag = reinterpret_cast<int *>(scr_lse + QROWS);
     StageMeta *meta = reinterpret_cast<StageMeta *>(reinterpret_cast<uint8_t *>(scratch) + align_up(Sh::SCRATCH, 128));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(meta + NST);
     uint64_t *empty_bar = full_bar + NST;
@@ -178,6 +198,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             prefetch_tensormap(&tmv);
         }
         const int B = p.B, Hkv = p.Hkv, C = p.chunk, ps = p.page_size, boxr = p.boxr;
+        // K/V are streamed once per call: keep them from displacing other lines in L2.
+        const uint64_t kv_policy = l2_policy_evict_first();
         const int BPT = TILE / boxr;  // boxes per tile: 1, 2, 4 (or 8)
         // Item counts per sequence and their prefix sums.
         int running = 0;
@@ -313,8 +335,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const int tok = (box0 + kb + lane) * boxr;
                     const int slot = tok % ps;
                     const uint32_t off = (uint32_t)(lane * NHALF * boxr * SUBROW);
-                    tma_load_5d(smem_u32(sb + off), &tmk, fb, 0, slot, 0, kvh, pg);
-                    tma_load_5d(smem_u32(sb + Sh::KV_REGION + off), &tmv, fb, 0, slot, 0, kvh, pg);
+                    tma_load_5d(smem_u32(sb + off), &tmk, fb, 0, slot, 0, kvh, pg, kv_policy);
+                    tma_load_5d(smem_u32(sb + Sh::KV_REGION + off), &tmv, fb, 0, slot, 0, kvh, pg, kv_policy);
                 }
                 ++n_issued;
                 if (++st == NST) { st = 0; ph ^= 1u; }
@@ -424,7 +446,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
         }
 
-#pragma unroll 1
+#pragma unroll
         for (int sub = 0; sub < SUBT; ++sub) {
         // This warp's 16 tokens: tile rows r0 .. r0+15, inside box r0 / boxr
         // (boxes hold NHALF swizzled regions of boxr rows x SUBROW bytes).
@@ -438,11 +460,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const int row_a = rib + (lane & 7) + ((lane >> 3) & 1) * 8;  // QK: ldmatrix rows
             const int row_t = rib + (lane & 7) + (lane >> 4) * 8;        // PV (f16/bf16): .trans rows
             // ---------------------------------------------------------- S = K Q^T
-            float sacc[NT][4];
+            // Two independent accumulator chains (even / odd k-steps) halve
+            // the dependent MMA latency of the dot products.
+            float sacc[NT][4], sacc2[NT][4];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) sacc[n][r] = 0.f;
+                for (int r = 0; r < 4; ++r) sacc[n][r] = sacc2[n][r] = 0.f;
             if constexpr (!FP8) {
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk) {
@@ -453,10 +477,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), a0, a1, a2, a3);
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
+                        float *acc = (kk & 1) ? sacc2[n] : sacc[n];
                         if constexpr (KV == KV_BF16)
-                            mma_bf16(sacc[n], a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                            mma_bf16(acc, a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
                         else
-                            mma_f16(sacc[n], a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                            mma_f16(acc, a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
                     }
                 }
             } else {
@@ -478,10 +503,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         mma_f16(sacc[n], a00, a01, a02, a03, qf[2 * jg][n][0], qf[2 * jg][n][1]);
-                        mma_f16(sacc[n], a10, a11, a12, a13, qf[2 * jg + 1][n][0], qf[2 * jg + 1][n][1]);
+                        mma_f16(sacc2[n], a10, a11, a12, a13, qf[2 * jg + 1][n][0], qf[2 * jg + 1][n][1]);
                     }
                 }
             }
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sacc[n][r] += sacc2[n][r];
 
             // ------------------------------------------------- online softmax (exp2)
             float sc = scale_log2;
@@ -655,43 +684,66 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         named_bar_sync(1, NC * 32);
         const int tid = warp * 32 + lane;
         const int G = p.G;
-        for (int idx = tid; idx < G * D; idx += NC * 32) {
-            const int h = idx / D, d = idx - h * D;
+        // Per head: combined max, the warps' weights (in place of their max)
+        // and the combined denominator; then the D outputs in float4 groups.
+        if (tid < G) {
+            const int h = tid;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NC; ++w) M = fmaxf(M, scr_m[w * QROWS + h]);
-            float acc = 0.f, Ls = 0.f;
-            if (M != -INFINITY) {
+            float Ls = 0.f;
 #pragma unroll
-                for (int w = 0; w < NC; ++w) {
-                    const float a = ex2(scr_m[w * QROWS + h] - M);
-                    acc += a * scratch[(w * QROWS + h) * SS + d];
-                    Ls += a * scr_l[w * QROWS + h];
-                }
+            for (int w = 0; w < NC; ++w) {
+                const float a = (M == -INFINITY) ? 0.f : ex2(scr_m[w * QROWS + h] - M);
+                scr_m[w * QROWS + h] = a;
+                Ls += a * scr_l[w * QROWS + h];
+            }
+            const bool empty = !(Ls > 0.f);
+            const size_t row = (size_t)mb * p.Hq + (size_t)m_kvh * G + h;
+            if (m_nsplit == 1) {
+                scr_inv[h] = empty ? 0.f : 1.f / Ls;
+                if (p.lse) p.lse[row] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+            } else {
+                scr_inv[h] = 1.f;
+                p.part_m[row * p.S + m_s] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+                p.part_d[row * p.S + m_s] = Ls;
+            }
+        }
+        named_bar_sync(1, NC * 32);
+        for (int idx = tid; idx < G * (D / 4); idx += NC * 32) {
+            const int h = idx / (D / 4), d = (idx - h * (D / 4)) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < NC; ++w) {
+                const float a = scr_m[w * QROWS + h];
+                const float4 v = *reinterpret_cast<const float4 *>(scratch + (w * QROWS + h) * SS + d);
+                acc.x = fmaf(a, v.x, acc.x);
+                acc.y = fmaf(a, v.y, acc.y);
+                acc.z = fmaf(a, v.z, acc.z);
+                acc.w = fmaf(a, v.w, acc.w);
             }
             const size_t row = (size_t)mb * p.Hq + (size_t)m_kvh * G + h;
             if (m_nsplit == 1) {
-                const bool empty = !(Ls > 0.f);
-                store_out(p.out, row * D + d, empty ? 0.f : acc / Ls, p.out_dtype);
-                if (d == 0 && p.lse) p.lse[row] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
+                const float inv = scr_inv[h];
+                store_out4(p.out, row * D + d, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.out_dtype);
             } else {
-                p.part_o[(row * p.S + m_s) * D + d] = acc;
-                if (d == 0) {
-                    p.part_m[row * p.S + m_s] = (M == -INFINITY) ? -INFINITY : M * kLn2;
-                    p.part_d[row * p.S + m_s] = Ls;
-                }
+                *reinterpret_cast<float4 *>(p.part_o + (row * p.S + m_s) * D + d) = acc;
             }
         }
         if (m_nsplit > 1 && p.fuse_merge) {
-            __threadfence();
+            // Publish the partial state: the barrier orders every consumer
+            // thread's stores before thread 0's device-scope fence and
+            // counter update (release); the CTA that sees the last count
+            // fences again (acquire) before reading the other partials.
             named_bar_sync(1, NC * 32);
             if (tid == 0) {
+                __threadfence();
                 const int prev = atomicAdd(p.merge_ctr + (size_t)mb * p.Hkv + m_kvh, 1);
+                __threadfence();
                 *scr_flag = (prev == m_nsplit - 1);
             }
             named_bar_sync(1, NC * 32);
             if (*scr_flag) {
-                __threadfence();
                 merge_group<NC>(p, mb, m_kvh, m_nsplit, scratch, warp, lane, D);
                 if (tid == 0) atomicExch(p.merge_ctr + (size_t)mb * p.Hkv + m_kvh, 0);
             }
