@@ -39,6 +39,7 @@
 
 namespace fd {
 
+constexpr int kOrderBuckets = 64;  // length buckets of the longest-first dispatch order (2 per lane)
 constexpr int kFlagFirst = 1;
 constexpr int kFlagLast = 2;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     fd_split_kv_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmv) {
     using Sh = DecodeShape<KV, D, NT, NC, SUBT>;
-    constexpr int TILE = Sh::TILE, E = Sh::E, SUBROW = Sh::SUBROW, NHALF = Sh::NHALF;
+    constexpr int TILE = Sh::TILE, SUBROW = Sh::SUBROW, NHALF = Sh::NHALF;
     constexpr int QROWS = Sh::QROWS, SS = Sh::SS;
     constexpr bool FP8 = (KV == KV_E4M3);
 
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     uint64_t *empty_bar = full_bar + NST;
     int *prefix = reinterpret_cast<int *>(empty_bar + NST);
     int *lens = prefix + p.B + 1;
+    int *order = lens + p.B;
+    int *hist = order + p.B;  // kOrderBuckets
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -201,11 +204,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // K/V are streamed once per call: keep them from displacing other lines in L2.
         const uint64_t kv_policy = l2_policy_evict_first();
         const int BPT = TILE / boxr;  // boxes per tile: 1, 2, 4 (or 8)
-        // Item counts per sequence and their prefix sums.
-        int running = 0;
+        // Dispatch order: sequences sorted longest first into kOrderBuckets
+        // length buckets (stable, identical in every CTA because it depends
+        // only on seq_lens), so the short items come last and fill the tail.
+        // Then the item counts in that order and their prefix sums.
+        for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
+        __syncwarp();
+        const long long cap1 = (long long)p.cap + 1;
         for (int base = 0; base < B; base += 32) {
             const int b = base + lane;
-            int v = 0;
+            int bucket = kOrderBuckets;  // sentinel for lanes past B
             if (b < B) {
                 int L = p.seq_lens[b];
                 if (L < 0 || L > p.cap) {
@@ -213,6 +221,47 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     L = L < 0 ? 0 : p.cap;
                 }
                 lens[b] = L;
+                bucket = (kOrderBuckets - 1) - (int)min((long long)(kOrderBuckets - 1), (L * (long long)kOrderBuckets) / cap1);
+            }
+            const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+            if (b < B && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+            __syncwarp();
+        }
+        {   // exclusive scan of the bucket counts (2 buckets per lane)
+            const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
+            int v = h0 + h1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            const int excl = v - h0 - h1;
+            __syncwarp();
+            hist[2 * lane] = excl;
+            hist[2 * lane + 1] = excl + h0;
+            __syncwarp();
+        }
+        for (int base = 0; base < B; base += 32) {
+            const int b = base + lane;
+            const int L = b < B ? lens[b] : 0;
+            const int bucket = b < B ? (kOrderBuckets - 1) - (int)min((long long)(kOrderBuckets - 1),
+                                                                  (L * (long long)kOrderBuckets) / cap1)
+                                     : kOrderBuckets;
+            const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+            if (b < B) {
+                const unsigned below = peers & ((1u << lane) - 1u);
+                order[hist[bucket] + __popc(below)] = b;
+            }
+            __syncwarp();
+            if (b < B && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+            __syncwarp();
+        }
+        int running = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int i = base + lane;
+            int v = 0;
+            if (i < B) {
+                const int L = lens[order[i]];
                 v = (L == 0 ? 1 : (L + C - 1) / C) * Hkv;
             }
 #pragma unroll
@@ -220,50 +269,78 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 const int t = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += t;
             }
-            if (b < B) prefix[b + 1] = running + v;
+            if (i < B) prefix[i + 1] = running + v;
             running += __shfl_sync(0xffffffffu, v, 31);
         }
         if (lane == 0) prefix[0] = 0;
         __syncwarp();
         const int total = running;
 
-        int st = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        long long n_issued = 0;
-        while (ok) {
-            int item = 0;
-            if (lane == 0) item = atomicAdd(p.work_ctr, 1);
-            item = __shfl_sync(0xffffffffu, item, 0);
-            if (item >= total) break;
+        // Item -> (b, split, kvh) and its token range.
+        struct Item {
+            int b, s, kvh, L, nsplit, t_begin, t_end, ntok, ntiles, nbox, box0;
+        };
+        auto decode_item = [&](int item) -> Item {
             int lo = 0, hi = B - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
             }
-            const int b = lo;
-            const int rem = item - prefix[b];
-            const int s = rem / Hkv, kvh = rem - (rem / Hkv) * Hkv;
-            const int L = lens[b];
-            const int nsplit = (prefix[b + 1] - prefix[b]) / Hkv;
-            const int t_begin = s * C;
-            const int t_end = min(L, t_begin + C);
-            const int ntok = max(0, t_end - t_begin);
-            const int ntiles = max(1, (ntok + TILE - 1) / TILE);
-            const int nbox = (ntok + boxr - 1) / boxr;
-            const int box0 = t_begin / boxr;
-            const int32_t *btrow = p.block_table + (size_t)b * p.max_blocks;
+            Item it;
+            it.b = order[lo];
+            const int rem = item - prefix[lo];
+            it.s = rem / Hkv;
+            it.kvh = rem - it.s * Hkv;
+            it.L = lens[it.b];
+            it.nsplit = (prefix[lo + 1] - prefix[lo]) / Hkv;
+            it.t_begin = it.s * C;
+            it.t_end = min(it.L, it.t_begin + C);
+            it.ntok = max(0, it.t_end - it.t_begin);
+            it.ntiles = max(1, (it.ntok + TILE - 1) / TILE);
+            it.nbox = (it.ntok + boxr - 1) / boxr;
+            it.box0 = it.t_begin / boxr;
+            return it;
+        };
+        // Page id of box k of an item (-1 past its end; -2 for a block-table
+        // column out of range).
+        auto page_of = [&](const Item &it, int k) -> int {
+            if (k >= it.nbox) return -1;
+            const int col = ((it.box0 + k) * boxr) / ps;
+            if (col >= p.max_blocks) return -2;
+            return __ldg(p.block_table + (size_t)it.b * p.max_blocks + col);
+        };
+        auto claim = [&]() -> int {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(p.work_ctr, 1);
+            return __shfl_sync(0xffffffffu, item, 0);
+        };
 
-            // Page id of box k of this item (-1 past the end; -2 for a
-            // table column out of range).
-            auto page_of = [&](int k) -> int {
-                if (k >= nbox) return -1;
-                const int col = ((box0 + k) * boxr) / ps;
-                if (col >= p.max_blocks) return -2;
-                return __ldg(btrow + col);
-            };
-            int pg_cur = page_of(lane);
-            int pg_nxt = page_of(32 + lane);
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        long long n_issued = 0;
+        // One item of lookahead: the next item is claimed, and its first two
+        // batches of page ids requested, while the current one streams.
+        int next_item = claim();
+        Item nx{};
+        int npg0 = -1, npg1 = -1;
+        if (next_item < total) {
+            nx = decode_item(next_item);
+            npg0 = page_of(nx, lane);
+            npg1 = page_of(nx, 32 + lane);
+        }
+        while (ok && next_item < total) {
+            const Item cur = nx;
+            int pg_cur = npg0, pg_nxt = npg1;
+            next_item = claim();
+            if (next_item < total) {
+                nx = decode_item(next_item);
+                npg0 = page_of(nx, lane);
+                npg1 = page_of(nx, 32 + lane);
+            }
+            const int b = cur.b, s = cur.s, kvh = cur.kvh, nsplit = cur.nsplit;
+            const int t_begin = cur.t_begin, t_end = cur.t_end, ntok = cur.ntok, ntiles = cur.ntiles;
+            const int nbox = cur.nbox, box0 = cur.box0;
             float ks_cur = 1.f, vs_cur = 1.f;
             if constexpr (FP8) {
                 if (pg_cur >= 0 && pg_cur < p.num_pages) {
@@ -277,7 +354,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 if (kb >= (batch + 1) * 32) {
                     ++batch;
                     pg_cur = pg_nxt;
-                    pg_nxt = page_of((batch + 1) * 32 + lane);
+                    pg_nxt = page_of(cur, (batch + 1) * 32 + lane);
                     if constexpr (FP8) {
                         if (pg_cur >= 0 && pg_cur < p.num_pages) {
                             ks_cur = __ldg(p.k_scale + (size_t)pg_cur * Hkv + kvh);
@@ -760,7 +837,7 @@ size_t decode_smem_for(int stages, int B) {
     n += align_up(Sh::SCRATCH, 128);
     n += (size_t)stages * sizeof(StageMeta);
     n += (size_t)stages * 16;
-    n += (size_t)(2 * B + 1) * 4;
+    n += (size_t)(3 * B + 1 + kOrderBuckets) * 4;
     return n;
 }
 

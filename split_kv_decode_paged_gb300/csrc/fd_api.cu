@@ -126,8 +126,11 @@ fd_status device_info(DeviceInfo &di) {
 int round_up(long long x, int a) { return (int)(((x + a - 1) / a) * a); }
 
 // Greedy list-scheduling estimate of the busiest CTA (in token-times) when
-// the items of chunk length C are handed out in b-major order to P CTAs.
-double makespan(const std::vector<int> &lens, int Hkv, int C, int P, double item_ovh) {
+// the items of chunk length C are handed out to P CTAs in the kernel's
+// dispatch order (sequences longest first, then split, then KV head).
+double makespan(const std::vector<int> &lens_in, int Hkv, int C, int P, double item_ovh) {
+    std::vector<int> lens(lens_in);
+    std::stable_sort(lens.begin(), lens.end(), [](int a, int b) { return a > b; });
     std::priority_queue<double, std::vector<double>, std::greater<double>> q;
     for (int i = 0; i < P; ++i) q.push(0.0);
     double worst = 0.0;
