@@ -192,14 +192,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         fence_barrier_init();
     }
+    if (warp == NC && lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
     __syncthreads();
+    // Everything above touches only this CTA's shared memory and the kernel
+    // parameters; global inputs and the workspace are read after the
+    // preceding grid (e.g. the previous decode call) has completed.
+    grid_dependency_wait();
 
     if (warp == NC) {
         // ================================================================ producer
-        if (lane == 0) {
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
-        }
         const int B = p.B, Hkv = p.Hkv, C = p.chunk, ps = p.page_size, boxr = p.boxr;
         // K/V are streamed once per call: keep them from displacing other lines in L2.
         const uint64_t kv_policy = l2_policy_evict_first();
@@ -419,6 +423,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 if (++st == NST) { st = 0; ph ^= 1u; }
             }
         }
+        // No more items to claim: the next grid in the stream may start
+        // launching onto SMs as they free up.
+        grid_launch_dependents();
         if (!ok) {
             // Abort: wait (bounded) for the copies still in flight into the
             // stages issued most recently before leaving.
@@ -847,8 +854,20 @@ cudaError_t launch_decode_t(const DecodeParams &dp, const CUtensorMap &tmk, cons
     auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, DecodeShape<KV, D, NT, NC, SUBT>::THREADS, smem, stream>>>(dp, tmk, tmv);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the kernel may begin its prologue while
+    // the previous grid in the stream drains; it waits (griddepcontrol.wait)
+    // before reading any global input.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(DecodeShape<KV, D, NT, NC, SUBT>::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, dp, tmk, tmv);
 }
 
 }  // namespace fd
