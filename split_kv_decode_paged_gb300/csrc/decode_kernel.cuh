@@ -313,9 +313,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             if (col >= p.max_blocks) return -2;
             return __ldg(p.block_table + (size_t)it.b * p.max_blocks + col);
         };
+        // Item ids: CTA i starts with item i; later items come from the
+        // atomic counter, offset by the grid size.
         auto claim = [&]() -> int {
             int item = 0;
-            if (lane == 0) item = atomicAdd(p.work_ctr, 1);
+            if (lane == 0) item = (int)gridDim.x + atomicAdd(p.work_ctr, 1);
             return __shfl_sync(0xffffffffu, item, 0);
         };
 
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         long long n_issued = 0;
         // One item of lookahead: the next item is claimed, and its first two
         // batches of page ids requested, while the current one streams.
-        int next_item = claim();
+        int next_item = (int)blockIdx.x;
         Item nx{};
         int npg0 = -1, npg1 = -1;
         if (next_item < total) {
