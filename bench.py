@@ -174,7 +174,9 @@ def l2_flush(buf):
     buf.zero_()
     sink = _flush_sink.setdefault(buf.device, torch.empty((), dtype=buf.dtype, device=buf.device))
     torch.sum(buf, dim=0, out=sink)
-wl, steps, warmup, flush, stream=None, **plan_opts):
+
+
+def time_decode(wl, steps, warmup, flush, stream=None, **plan_opts):
     import split_kv_decode_paged_gb300 as fd
     dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu(), **plan_opts)
     out = torch.empty_like(wl.q)

@@ -161,6 +161,35 @@ fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pa
                           float *lse, void *workspace, size_t workspace_bytes,
                           int32_t *status_dev, void *stream);
 
+/* Optional indirections of a decode call ("Inference Cookbook" §5.2
+ * cache_batch_idx, §5.3 cache_leftpad).  All device pointers, NULL = off.
+ *   cache_batch_idx  int32 [B]: q row b reads cache row cache_batch_idx[b]
+ *                    (its block-table row, seq_lens entry and leftpad entry);
+ *                    out/lse stay indexed by q row.  Lets the active subset
+ *                    of a larger batch decode without copying its metadata.
+ *   cache_leftpad    int32 [cache rows]: the first cached token of the row;
+ *                    q row b attends tokens [leftpad[cb], seq_lens[cb]).
+ *   cache_rows       rows of block_table / seq_lens / cache_leftpad when
+ *                    cache_batch_idx is set (an index outside [0, cache_rows)
+ *                    sets FD_DEV_BAD_PAGE and that row gets out = 0, lse = -inf).
+ * Plan such a call with the attended lengths seq_lens[cb] - leftpad[cb] of
+ * the q rows as seq_lens_host; a leftpad outside [0, seq_len] sets
+ * FD_DEV_CAPACITY. */
+typedef struct {
+    const int32_t *cache_batch_idx;
+    const int32_t *cache_leftpad;
+    int cache_rows;
+} fd_decode_extras;
+
+/* fd_decode_paged with the indirections of fd_decode_extras (NULL extras is
+ * the plain call).  Same arguments, errors and guarantees otherwise. */
+fd_status fd_decode_paged_ex(const fd_plan_t *plan, const void *q, const void *k_pages,
+                             const void *v_pages, const float *k_scale, const float *v_scale,
+                             const int32_t *block_table, const int32_t *seq_lens,
+                             const fd_decode_extras *extras, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                             void *stream);
+
 /* Merge S partial states per (b, hq) into the output [P1 §2.1 step 3 merge;
  * P2 stage two].
  *   o_part   device fp32 [B, Hq, S, D]: unnormalised sum_t exp(s_t - m) v_t

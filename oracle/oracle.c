@@ -313,6 +313,51 @@ int orc_decode_paged_pairs(const orc_problem *p, const void *q, const void *k_pa
     return run_threads(&in, seq_lens, pairs, npairs, out, lse, nthreads);
 }
 
+/* Cookbook §5.2-5.3: indirection to a cache row and a left offset.  The
+ * gather of each token is the paged gather above, for the cache row's block
+ * table; the softmax is the same definition over the attended range. */
+int orc_decode_paged_ex(const orc_problem *p, int cache_rows, const int32_t *cache_batch_idx,
+                        const int32_t *cache_leftpad, const void *q, const void *k_pages,
+                        const void *v_pages, const float *k_scale, const float *v_scale,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        double *out, double *lse) {
+    if (check_problem(p) || cache_rows < 1) return ORC_ERR_ARG;
+    if (p->kv_dtype == ORC_E4M3 && (!k_scale || !v_scale)) return ORC_ERR_ARG;
+    orc_problem pc = *p;
+    pc.B = cache_rows;
+    for (int b = 0; b < p->B; ++b) {
+        int cb = cache_batch_idx ? cache_batch_idx[b] : b;
+        if (cb < 0 || cb >= cache_rows) return ORC_ERR_ARG;
+        int L = seq_lens[cb];
+        int lp = cache_leftpad ? cache_leftpad[cb] : 0;
+        if (lp < 0 || lp > L) return ORC_ERR_ARG;
+        for (int hq = 0; hq < p->Hq; ++hq) {
+            /* q row b of the caller, keys/values of cache row cb */
+            const int D = p->D;
+            double *o = out + ((size_t)b * p->Hq + hq) * D;
+            orc_inputs in = {&pc, NULL, k_pages, v_pages, k_scale, v_scale, block_table, NULL, NULL, 0};
+            /* a q buffer view holding only row b at index cb */
+            size_t esz = p->q_dtype == ORC_F32 ? 4 : 2;
+            void *qv = calloc((size_t)cache_rows * p->Hq * D, esz);
+            if (!qv) return ORC_ERR_NOMEM;
+            memcpy((char *)qv + ((size_t)cb * p->Hq + hq) * D * esz,
+                   (const char *)q + ((size_t)b * p->Hq + hq) * D * esz, D * esz);
+            in.q = qv;
+            double m, z;
+            int rc = partial(&in, cb, hq, lp, L, o, &m, &z);
+            free(qv);
+            if (rc) return rc;
+            if (L - lp == 0) {
+                lse[(size_t)b * p->Hq + hq] = -INFINITY;
+                continue;
+            }
+            for (int d = 0; d < D; ++d) o[d] /= z;
+            lse[(size_t)b * p->Hq + hq] = m + log(z);
+        }
+    }
+    return ORC_OK;
+}
+
 int orc_decode_contiguous(const orc_problem *p, int max_seqlen, const void *q,
                           const void *k_cache, const void *v_cache,
                           const int32_t *seq_lens, double *out, double *lse) {

@@ -82,6 +82,18 @@ int orc_decode_paged_pairs(const orc_problem *p, const void *q, const void *k_pa
                            const int32_t *pairs, int npairs,
                            double *out, double *lse, int nthreads);
 
+/* Decode with the "Inference Cookbook" §5.2-5.3 indirections: q row b reads
+ * cache row cb = cache_batch_idx[b] (identity when NULL) -- its block-table
+ * row, seq_lens entry and leftpad entry -- and attends tokens
+ * [leftpad[cb], seq_lens[cb]) (leftpad 0 when NULL).  cache_rows = rows of
+ * block_table / seq_lens / leftpad.  Returns ORC_ERR_ARG for an index outside
+ * the cache or a leftpad outside [0, seq_len]. */
+int orc_decode_paged_ex(const orc_problem *p, int cache_rows, const int32_t *cache_batch_idx,
+                        const int32_t *cache_leftpad, const void *q, const void *k_pages,
+                        const void *v_pages, const float *k_scale, const float *v_scale,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        double *out, double *lse);
+
 /* Contiguous-cache decode: k/v_cache [B, max_seqlen, Hkv, D] (kv_dtype, no
  * scales).  The comparator for the paged gather. */
 int orc_decode_contiguous(const orc_problem *p, int max_seqlen, const void *q,

@@ -47,6 +47,8 @@ def lib():
         L.orc_decode_paged_pairs.restype = I
         L.orc_decode_paged_pairs.argtypes = [ctypes.POINTER(Problem), P, P, P, P, P, P, P,
                                              P, I, P, P, I]
+        L.orc_decode_paged_ex.restype = I
+        L.orc_decode_paged_ex.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P, P, P, P, P, P]
         L.orc_decode_contiguous.restype = I
         L.orc_decode_contiguous.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P]
         L.orc_partial_state.restype = I
@@ -135,6 +137,22 @@ def decode_paged_pairs(p, q, k_pages, v_pages, k_scale, v_scale, block_table, se
                                       _ptr(vs), _ptr(bt), _ptr(sl), _ptr(pr), n, _ptr(out),
                                       _ptr(lse), int(nthreads))
     _check(rc, "decode_paged_pairs")
+    return out, lse
+
+
+def decode_paged_ex(p, cache_rows, cache_batch_idx, cache_leftpad, q, k_pages, v_pages, k_scale, v_scale,
+                    block_table, seq_lens):
+    """Decode with cache-row indirection and left padding; p.B = q rows."""
+    q, k, v = raw(q), raw(k_pages), raw(v_pages)
+    ks, vs = raw(k_scale), raw(v_scale)
+    bt, sl = raw(block_table).astype(np.int32), raw(seq_lens).astype(np.int32)
+    bi = None if cache_batch_idx is None else raw(cache_batch_idx).astype(np.int32)
+    lp = None if cache_leftpad is None else raw(cache_leftpad).astype(np.int32)
+    out = np.zeros((p.B, p.Hq, p.D), np.float64)
+    lse = np.zeros((p.B, p.Hq), np.float64)
+    rc = lib().orc_decode_paged_ex(ctypes.byref(p), int(cache_rows), _ptr(bi), _ptr(lp), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), _ptr(out), _ptr(lse))
+    _check(rc, "decode_paged_ex")
     return out, lse
 
 

@@ -21,8 +21,8 @@ FD_ERR_BAD_PAGE, FD_ERR_CUDA, FD_ERR_CAPACITY, FD_ERR_TIMEOUT = 4, 5, 6, 7
 FD_DEV_BAD_PAGE, FD_DEV_CAPACITY, FD_DEV_TIMEOUT = 0x1, 0x2, 0x4
 FD_F16, FD_BF16, FD_E4M3, FD_F32 = 0, 1, 2, 3
 
-EXPORTS = ("fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string",
-           "fd_status_from_device", "fd_api_version")
+EXPORTS = ("fd_plan", "fd_decode_paged", "fd_decode_paged_ex", "fd_merge_states", "fd_append_kv",
+           "fd_status_string", "fd_status_from_device", "fd_api_version")
 
 _TORCH_TO_FD = {torch.float16: FD_F16, torch.bfloat16: FD_BF16, torch.float8_e4m3fn: FD_E4M3,
                 torch.float32: FD_F32}
@@ -51,6 +51,11 @@ class FdPlanOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("num_sms", ctypes.c_int), ("fuse_merge", ctypes.c_int),
                 ("max_seq_len", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("split_margin_pct", ctypes.c_int),
                 ("tile_tokens", ctypes.c_int)]
+
+
+class FdDecodeExtras(ctypes.Structure):
+    _fields_ = [("cache_batch_idx", ctypes.c_void_p), ("cache_leftpad", ctypes.c_void_p),
+                ("cache_rows", ctypes.c_int)]
 
 
 class FdPlan(ctypes.Structure):
@@ -82,6 +87,9 @@ def load(path: str = LIB_PATH):
     L.fd_plan.argtypes = [ctypes.POINTER(FdProblem), P, ctypes.POINTER(FdPlanOptions), ctypes.POINTER(FdPlan)]
     L.fd_decode_paged.restype = I
     L.fd_decode_paged.argtypes = [ctypes.POINTER(FdPlan), P, P, P, P, P, P, P, P, P, P, S, P, P]
+    L.fd_decode_paged_ex.restype = I
+    L.fd_decode_paged_ex.argtypes = [ctypes.POINTER(FdPlan), P, P, P, P, P, P, P, ctypes.POINTER(FdDecodeExtras),
+                                     P, P, P, S, P, P]
     L.fd_merge_states.restype = I
     L.fd_merge_states.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
     L.fd_append_kv.restype = I
@@ -152,6 +160,18 @@ def fd_decode_paged(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, block_t
                                 _ptr(status), _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged")
+
+
+def fd_decode_paged_ex(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
+                       workspace, cache_batch_idx=None, cache_leftpad=None, cache_rows=0, status=None, stream=None):
+    ex = FdDecodeExtras(None if cache_batch_idx is None else cache_batch_idx.data_ptr(),
+                        None if cache_leftpad is None else cache_leftpad.data_ptr(), int(cache_rows))
+    rc = load().fd_decode_paged_ex(ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
+                                   _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), ctypes.byref(ex), _ptr(out),
+                                   _ptr(lse), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                   _ptr(status), _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_decode_paged_ex")
 
 
 def fd_merge_states(o_part, m, d, out, lse=None, stream=None):

@@ -45,7 +45,7 @@ constexpr int kFlagLast = 2;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct StageMeta {
-    int b, kvh, s, t0, nvalid, flags, nsplit, pad;
+    int b, kvh, s, t0, nvalid, flags, nsplit, vlo;  // valid tile rows: [vlo, nvalid)
     float kscale[kMaxBoxesPerTile];
     float vscale[kMaxBoxesPerTile];
 };
@@ -208,6 +208,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // K/V are streamed once per call: keep them from displacing other lines in L2.
         const uint64_t kv_policy = l2_policy_evict_first();
         const int BPT = TILE / boxr;  // boxes per tile: 1, 2, 4 (or 8)
+        // Cache row of q row b (block table, seq_lens and leftpad are
+        // indexed by it); -1 for an index outside the cache (flagged).
+        auto cache_row = [&](int b) -> int {
+            if (!p.batch_idx) return b;
+            const int cb = __ldg(p.batch_idx + b);
+            if (cb < 0 || cb >= p.cache_rows) {
+                flag_status(p.status, FD_DEV_BAD_PAGE);
+                return -1;
+            }
+            return cb;
+        };
         // Dispatch order: sequences sorted longest first into kOrderBuckets
         // length buckets (stable, identical in every CTA because it depends
         // only on seq_lens), so the short items come last and fill the tail.
@@ -219,7 +230,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const int b = base + lane;
             int bucket = kOrderBuckets;  // sentinel for lanes past B
             if (b < B) {
-                int L = p.seq_lens[b];
+                // Attended length: tokens [leftpad, seq_len) of the q row's cache row.
+                const int cb = cache_row(b);
+                int L = 0;
+                if (cb >= 0) {
+                    L = p.seq_lens[cb];
+                    if (p.leftpad) {
+                        const int lp = p.leftpad[cb];
+                        L = (lp < 0 || lp > L) ? -1 : L - lp;
+                    }
+                }
                 if (L < 0 || L > p.cap) {
                     flag_status(p.status, FD_DEV_CAPACITY);
                     L = L < 0 ? 0 : p.cap;
@@ -281,8 +301,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const int total = running;
 
         // Item -> (b, split, kvh) and its token range.
+        // Tokens [t_begin, t_end) of cache row cb; tiles start at the box
+        // boundary a <= t_begin, and the first tile masks its vlo leading rows.
         struct Item {
-            int b, s, kvh, L, nsplit, t_begin, t_end, ntok, ntiles, nbox, box0;
+            int b, cb, s, kvh, L, nsplit, t_begin, t_end, ntok, ntiles, nbox, box0, vlo;
         };
         auto decode_item = [&](int item) -> Item {
             int lo = 0, hi = B - 1;
@@ -297,12 +319,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             it.kvh = rem - it.s * Hkv;
             it.L = lens[it.b];
             it.nsplit = (prefix[lo + 1] - prefix[lo]) / Hkv;
-            it.t_begin = it.s * C;
-            it.t_end = min(it.L, it.t_begin + C);
+            it.cb = it.b;
+            int lp = 0;
+            if (p.batch_idx) {
+                it.cb = __ldg(p.batch_idx + it.b);
+                if (it.cb < 0 || it.cb >= p.cache_rows) { it.cb = 0; it.L = 0; }
+            }
+            if (p.leftpad && it.L > 0) lp = __ldg(p.leftpad + it.cb);
+            it.t_begin = lp + it.s * C;
+            it.t_end = lp + min(it.L, it.s * C + C);
             it.ntok = max(0, it.t_end - it.t_begin);
-            it.ntiles = max(1, (it.ntok + TILE - 1) / TILE);
-            it.nbox = (it.ntok + boxr - 1) / boxr;
-            it.box0 = it.t_begin / boxr;
+            const int a = it.ntok > 0 ? (it.t_begin / boxr) * boxr : it.t_begin;
+            it.vlo = it.t_begin - a;
+            const int span = it.ntok > 0 ? it.t_end - a : 0;
+            it.ntiles = max(1, (span + TILE - 1) / TILE);
+            it.nbox = (span + boxr - 1) / boxr;
+            it.box0 = a / boxr;
+            it.t_begin = a;  // tiles are laid out from the aligned start
             return it;
         };
         // Page id of box k of an item (-1 past its end; -2 for a block-table
@@ -311,7 +344,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             if (k >= it.nbox) return -1;
             const int col = ((it.box0 + k) * boxr) / ps;
             if (col >= p.max_blocks) return -2;
-            return __ldg(p.block_table + (size_t)it.b * p.max_blocks + col);
+            return __ldg(p.block_table + (size_t)it.cb * p.max_blocks + col);
         };
         // Item ids: CTA i starts with item i; later items come from the
         // atomic counter, offset by the grid size.
@@ -393,6 +426,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 if (lane == 0) {
                     m->b = b; m->kvh = kvh; m->s = s; m->t0 = t0;
                     m->nvalid = max(0, min(TILE, t_end - t0));
+                    m->vlo = j == 0 ? cur.vlo : 0;
                     m->flags = (j == 0 ? kFlagFirst : 0) | (j == ntiles - 1 ? kFlagLast : 0);
                     m->nsplit = nsplit;
                 }
@@ -477,7 +511,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const StageMeta &mt = meta[st];
         const int mb = mt.b;
         if (mb < 0) break;
-        const int flags = mt.flags, nvalid = mt.nvalid;
+        const int flags = mt.flags, nvalid = mt.nvalid, vlo = mt.vlo;
         const uint8_t *sb = stages + (size_t)st * Sh::STAGE;
         const uint32_t kbase = smem_u32(sb), vbase = kbase + Sh::KV_REGION, qbase = kbase + 2 * Sh::KV_REGION;
 
@@ -537,8 +571,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // This warp's 16 tokens: tile rows r0 .. r0+15, inside box r0 / boxr
         // (boxes hold NHALF swizzled regions of boxr rows x SUBROW bytes).
         const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+        // Valid rows of this sub-tile: [lo_loc, nloc) (lo_loc > 0 only at the
+        // start of an item that begins inside a box).
         const int nloc = max(0, min(kTokensPerWarp, nvalid - r0));
-        if (nloc > 0) {
+        const int lo_loc = max(0, vlo - r0);
+        if (nloc > lo_loc) {
             const int rib = r0 % p.boxr;  // first row inside the box (multiple of 16)
             const uint32_t hstride = (uint32_t)(p.boxr * SUBROW);
             const uint32_t box_off = (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
@@ -601,7 +638,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             // ------------------------------------------------- online softmax (exp2)
             float sc = scale_log2;
             if constexpr (FP8) sc *= mt.kscale[r0 / p.boxr];
-            const bool v0 = g < nloc, v1 = (g + 8) < nloc;
+            const bool v0 = g >= lo_loc && g < nloc, v1 = (g + 8) >= lo_loc && (g + 8) < nloc;
             float alpha[NT][2];
             uint32_t pb[NT][2];
             uint32_t pl[NT][2];  // bf16 V: low parts of the weights (P = hi + lo)
@@ -666,9 +703,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 
             // ---------------------------------------------------- O^T += V^T P^T
             uint32_t msk01 = 0xffffffffu, msk23 = 0xffffffffu;
-            if (nloc < kTokensPerWarp) {
-                msk01 = ((2 * c) < nloc ? 0x0000ffffu : 0u) | ((2 * c + 1) < nloc ? 0xffff0000u : 0u);
-                msk23 = ((2 * c + 8) < nloc ? 0x0000ffffu : 0u) | ((2 * c + 9) < nloc ? 0xffff0000u : 0u);
+            if (nloc < kTokensPerWarp || lo_loc > 0) {
+                auto ok_t = [&](int t) { return t >= lo_loc && t < nloc; };
+                msk01 = (ok_t(2 * c) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 1) ? 0xffff0000u : 0u);
+                msk23 = (ok_t(2 * c + 8) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 9) ? 0xffff0000u : 0u);
             }
             if constexpr (!FP8) {
 #pragma unroll

@@ -352,10 +352,14 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     return FD_OK;
 }
 
-fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pages, const void *v_pages,
-                          const float *k_scale, const float *v_scale, const int32_t *block_table,
-                          const int32_t *seq_lens, void *out, float *lse, void *workspace, size_t workspace_bytes,
-                          int32_t *status_dev, void *stream) {
+}  // extern "C"
+
+namespace {
+
+fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages, const void *v_pages,
+                      const float *k_scale, const float *v_scale, const int32_t *block_table,
+                      const int32_t *seq_lens, const fd_decode_extras *ex, void *out, float *lse, void *workspace,
+                      size_t workspace_bytes, int32_t *status_dev, void *stream) {
     if (!plan) return FD_ERR_INVALID_ARG;
     const fd_problem &p = plan->problem;
     fd_status st = validate_problem(&p);
@@ -385,6 +389,9 @@ fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pa
     dp.q = q;
     dp.block_table = block_table;
     dp.seq_lens = seq_lens;
+    dp.batch_idx = ex ? ex->cache_batch_idx : nullptr;
+    dp.leftpad = ex ? ex->cache_leftpad : nullptr;
+    dp.cache_rows = (ex && ex->cache_batch_idx) ? ex->cache_rows : p.B;
     dp.k_scale = k_scale;
     dp.v_scale = v_scale;
     dp.out = out;
@@ -425,6 +432,9 @@ fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pa
         mp.out = out;
         mp.lse = lse;
         mp.seq_lens = seq_lens;
+        mp.batch_idx = dp.batch_idx;
+        mp.leftpad = dp.leftpad;
+        mp.cache_rows = dp.cache_rows;
         mp.B = p.B;
         mp.Hq = p.Hq;
         mp.S = plan->num_splits;
@@ -436,6 +446,32 @@ fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pa
         if (e != cudaSuccess) return FD_ERR_CUDA;
     }
     return FD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fd_status fd_decode_paged(const fd_plan_t *plan, const void *q, const void *k_pages, const void *v_pages,
+                          const float *k_scale, const float *v_scale, const int32_t *block_table,
+                          const int32_t *seq_lens, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                          int32_t *status_dev, void *stream) {
+    return decode_impl(plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, nullptr, out, lse,
+                       workspace, workspace_bytes, status_dev, stream);
+}
+
+fd_status fd_decode_paged_ex(const fd_plan_t *plan, const void *q, const void *k_pages, const void *v_pages,
+                             const float *k_scale, const float *v_scale, const int32_t *block_table,
+                             const int32_t *seq_lens, const fd_decode_extras *extras, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream) {
+    if (extras) {
+        if (extras->cache_batch_idx && extras->cache_rows < 1) return FD_ERR_INVALID_ARG;
+        if ((extras->cache_batch_idx && !aligned(extras->cache_batch_idx, 4)) ||
+            (extras->cache_leftpad && !aligned(extras->cache_leftpad, 4)))
+            return FD_ERR_INVALID_ARG;
+    }
+    return decode_impl(plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, extras, out, lse,
+                       workspace, workspace_bytes, status_dev, stream);
 }
 
 fd_status fd_merge_states(const float *o_part, const float *m, const float *d, int B, int Hq, int S, int D,
@@ -454,6 +490,9 @@ fd_status fd_merge_states(const float *o_part, const float *m, const float *d, i
     mp.out = out;
     mp.lse = lse;
     mp.seq_lens = nullptr;
+    mp.batch_idx = nullptr;
+    mp.leftpad = nullptr;
+    mp.cache_rows = 0;
     mp.B = B;
     mp.Hq = Hq;
     mp.S = S;

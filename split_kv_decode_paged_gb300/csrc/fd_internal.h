@@ -25,6 +25,9 @@ struct DecodeParams {
     const void *q;             // [B, Hq, D]
     const int32_t *block_table;
     const int32_t *seq_lens;
+    const int32_t *batch_idx;  // [B] cache row of q row b, or null (row b)
+    const int32_t *leftpad;    // [cache rows] first attended token, or null (0)
+    int cache_rows;            // rows of block_table / seq_lens / leftpad
     const float *k_scale;      // [num_pages, Hkv] or null
     const float *v_scale;
     void *out;                 // [B, Hq, D]
@@ -54,6 +57,9 @@ struct MergeParams {
     void *out;
     float *lse;
     const int32_t *seq_lens;   // non-null: per-sequence split counts from lengths
+    const int32_t *batch_idx;  // as in DecodeParams (with seq_lens only)
+    const int32_t *leftpad;
+    int cache_rows;
     int B, Hq, S, D, chunk, cap;
     int out_dtype;
 };

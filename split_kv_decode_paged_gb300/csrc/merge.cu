@@ -31,7 +31,16 @@ __global__ void __launch_bounds__(kMergeThreads) fd_merge_states_kernel(const Me
     if (p.seq_lens) {
         // Rows of sequences that were not split were written by the decode
         // kernel itself; only the split ones are merged here.
-        int L = p.seq_lens[b];
+        int cb = b;
+        if (p.batch_idx) {
+            cb = p.batch_idx[b];
+            if (cb < 0 || cb >= p.cache_rows) return;
+        }
+        int L = p.seq_lens[cb];
+        if (p.leftpad) {
+            const int lp = p.leftpad[cb];
+            L = (lp < 0 || lp > L) ? 0 : L - lp;
+        }
         L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
         n = (L == 0) ? 1 : (L + p.chunk - 1) / p.chunk;
         if (n <= 1) return;
