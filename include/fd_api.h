@@ -253,6 +253,27 @@ fd_status fd_decode_paged_noalloc(const fd_plan_t *plan, const void *q, const vo
                                   const int32_t *seq_lens, void *out, float *lse,
                                   int32_t *status_dev, void *stream);
 
+/* fd_append_kv with rotary position embedding fused in ("Inference Cookbook"
+ * §3.4: the new key is rotated before it is written, so the cache holds
+ * rotated keys; the query is rotated at the same position).
+ *   rotary_cos, rotary_sin  device fp32 [max_pos, rotary_dim / 2]
+ *   rotary_dim              even, <= D: the first rotary_dim elements rotate
+ *   interleaved             0: pairs (i, i + rotary_dim/2) (GPT-NeoX style);
+ *                           1: pairs (2i, 2i+1)
+ *   q_inout                 device [B, Hq, D] in q_dtype rotated in place, or NULL
+ * Position = seq_lens[b].  Pair (x1, x2) at angle index i becomes
+ * ((x1*cos) - (x2*sin), (x2*cos) + (x1*sin)), each product and sum rounded to
+ * fp32, then rounded to the storage type (RNE; E4M3 caches quantise the
+ * rotated value as fd_append_kv does).  V is copied unrotated.  A sequence
+ * whose position is >= max_pos is skipped and sets FD_DEV_CAPACITY.
+ * seq_lens is not advanced. */
+fd_status fd_append_kv_rotary(const fd_problem *problem, const void *k_new, const void *v_new,
+                              void *k_pages, void *v_pages, const float *k_scale,
+                              const float *v_scale, const int32_t *block_table,
+                              const int32_t *seq_lens, const float *rotary_cos,
+                              const float *rotary_sin, int rotary_dim, int max_pos,
+                              int interleaved, void *q_inout, int32_t *status_dev, void *stream);
+
 /* Map a device status word to a status code (FD_OK when zero). */
 fd_status fd_status_from_device(int32_t status_word);
 

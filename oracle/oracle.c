@@ -441,3 +441,112 @@ int orc_append_kv(const orc_problem *p, int new_dtype, const void *k_new, const 
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------- rotary */
+
+void orc_rotary_f32(const float *x, int n, int rotary_dim, int interleaved, const float *cos_tab,
+                    const float *sin_tab, int pos, float *y) {
+    for (int d = 0; d < n; ++d) y[d] = x[d];
+    int half = rotary_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        int a = interleaved ? 2 * i : i;
+        int b = interleaved ? 2 * i + 1 : i + half;
+        float c = cos_tab[(size_t)pos * half + i];
+        float s = sin_tab[(size_t)pos * half + i];
+        float x1 = x[a], x2 = x[b];
+        float p1 = x1 * c, p2 = x2 * s, p3 = x2 * c, p4 = x1 * s;
+        y[a] = p1 - p2;
+        y[b] = p3 + p4;
+    }
+}
+
+/* Round-to-nearest-even of a finite or non-finite float to bfloat16 / f16
+ * bits, from the formats' definitions (exhaustive search is not needed:
+ * the conversions are exact rounding of the binary32 significand). */
+static uint16_t to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40); /* NaN stays NaN */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;                                                      /* ties to even */
+    return (uint16_t)(u >> 16);
+}
+
+static uint16_t to_f16_bits(float f) {
+    /* nearest representable binary16 by search over the neighbours of the
+     * double-precision value: decode candidates and pick the closest, ties
+     * to the even code. */
+    if (isnan(f)) return 0x7e00;
+    double v = (double)f;
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00);  /* rounds to infinity */
+    int best = 0;
+    double best_diff = INFINITY;
+    for (int code = 0; code < 0x7c00; ++code) {
+        double diff = fabs(a - orc_f16_to_double((uint16_t)code));
+        if (diff < best_diff || (diff == best_diff && (code & 1) == 0)) {
+            best = code;
+            best_diff = diff;
+        }
+        if (orc_f16_to_double((uint16_t)code) > a && diff > best_diff) break;
+    }
+    return (uint16_t)(sign | best);
+}
+
+static void store_16(void *base, int dtype, size_t idx, float v) {
+    ((uint16_t *)base)[idx] = dtype == ORC_BF16 ? to_bf16_bits(v) : to_f16_bits(v);
+}
+
+int orc_append_kv_rotary(const orc_problem *p, int new_dtype, const void *k_new, const void *v_new,
+                         void *k_pages, void *v_pages, const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         const float *cos_tab, const float *sin_tab, int rotary_dim, int max_pos,
+                         int interleaved, void *q_inout) {
+    if (check_problem(p) || !cos_tab || !sin_tab || rotary_dim < 2 || rotary_dim % 2 || rotary_dim > p->D ||
+        max_pos < 1)
+        return ORC_ERR_ARG;
+    int fp8 = p->kv_dtype == ORC_E4M3;
+    if (!fp8 && new_dtype != p->kv_dtype) return ORC_ERR_ARG;
+    if (fp8 && ((!k_scale || !v_scale) || (new_dtype != ORC_F16 && new_dtype != ORC_BF16))) return ORC_ERR_ARG;
+    if (new_dtype != ORC_F16 && new_dtype != ORC_BF16) return ORC_ERR_ARG;
+    int D = p->D;
+    float *x = (float *)malloc(sizeof(float) * D), *y = (float *)malloc(sizeof(float) * D);
+    if (!x || !y) { free(x); free(y); return ORC_ERR_NOMEM; }
+    int rc = ORC_OK;
+    for (int b = 0; b < p->B && rc == ORC_OK; ++b) {
+        int L = seq_lens[b];
+        if (L < 0 || L >= max_pos || L / p->page_size >= p->max_blocks_per_seq) { rc = ORC_ERR_BAD_PAGE; break; }
+        int page = block_table[(size_t)b * p->max_blocks_per_seq + L / p->page_size];
+        if (page < 0 || page >= p->num_pages) { rc = ORC_ERR_BAD_PAGE; break; }
+        int slot = L % p->page_size;
+        for (int kvh = 0; kvh < p->Hkv; ++kvh) {
+            size_t src = ((size_t)b * p->Hkv + kvh) * D;
+            size_t dst = (((size_t)page * p->page_size + slot) * p->Hkv + kvh) * (size_t)D;
+            for (int which = 0; which < 2; ++which) {
+                const void *in = which ? v_new : k_new;
+                void *pool = which ? v_pages : k_pages;
+                for (int d = 0; d < D; ++d) x[d] = (float)load_elem(in, new_dtype, src + d);
+                if (which == 0) orc_rotary_f32(x, D, rotary_dim, interleaved, cos_tab, sin_tab, L, y);
+                else memcpy(y, x, sizeof(float) * D);
+                if (!fp8) {
+                    for (int d = 0; d < D; ++d) store_16(pool, p->kv_dtype, dst + d, y[d]);
+                } else {
+                    float sc = (which ? v_scale : k_scale)[(size_t)page * p->Hkv + kvh];
+                    for (int d = 0; d < D; ++d) ((uint8_t *)pool)[dst + d] = orc_e4m3_from_float(y[d] / sc);
+                }
+            }
+        }
+        if (q_inout) {
+            for (int hq = 0; hq < p->Hq; ++hq) {
+                size_t off = ((size_t)b * p->Hq + hq) * D;
+                for (int d = 0; d < D; ++d) x[d] = (float)load_elem(q_inout, p->q_dtype, off + d);
+                orc_rotary_f32(x, D, rotary_dim, interleaved, cos_tab, sin_tab, L, y);
+                for (int d = 0; d < D; ++d) store_16(q_inout, p->q_dtype, off + d, y[d]);
+            }
+        }
+    }
+    free(x);
+    free(y);
+    return rc;
+}

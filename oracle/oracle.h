@@ -122,6 +122,27 @@ int orc_append_kv(const orc_problem *p, int new_dtype, const void *k_new, const 
                   void *k_pages, void *v_pages, const float *k_scale, const float *v_scale,
                   const int32_t *block_table, const int32_t *seq_lens);
 
+/* Rotary position embedding applied at append time ("Inference Cookbook"
+ * §3.4: the new key is rotated before it is written into the cache, and the
+ * query is rotated at the same position).  cos_tab/sin_tab: fp32
+ * [max_pos, rotary_dim / 2].  Pair (i, i + rotary_dim/2) (interleaved == 0,
+ * GPT-NeoX style) or (2i, 2i+1) (interleaved != 0) of the first rotary_dim
+ * elements is rotated by angle index i at position pos:
+ *   y1 = (x1 * cos) - (x2 * sin),  y2 = (x2 * cos) + (x1 * sin)
+ * with every product and sum rounded to fp32 (no fused multiply-add); the
+ * other elements pass through.  x: n fp32 values, y: n fp32 values. */
+void orc_rotary_f32(const float *x, int n, int rotary_dim, int interleaved, const float *cos_tab,
+                    const float *sin_tab, int pos, float *y);
+
+/* orc_append_kv with the key rotated (V is not) before it is stored, and q
+ * [B, Hq, D] (q_dtype, may be NULL) rotated in place, both at position
+ * seq_lens[b].  Rotated 16-bit values are rounded to nearest even. */
+int orc_append_kv_rotary(const orc_problem *p, int new_dtype, const void *k_new, const void *v_new,
+                         void *k_pages, void *v_pages, const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         const float *cos_tab, const float *sin_tab, int rotary_dim, int max_pos,
+                         int interleaved, void *q_inout);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,6 +49,10 @@ def lib():
                                              P, I, P, P, I]
         L.orc_decode_paged_ex.restype = I
         L.orc_decode_paged_ex.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P, P, P, P, P, P]
+        L.orc_rotary_f32.restype = None
+        L.orc_rotary_f32.argtypes = [P, I, I, I, P, P, I, P]
+        L.orc_append_kv_rotary.restype = I
+        L.orc_append_kv_rotary.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P, P, P, P, P, I, I, I, P]
         L.orc_decode_contiguous.restype = I
         L.orc_decode_contiguous.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P]
         L.orc_partial_state.restype = I
@@ -219,3 +223,30 @@ def e4m3_to_double(bits):
 
 def e4m3_from_float(x):
     return int(lib().orc_e4m3_from_float(float(x)))
+
+
+def rotary_f32(x, rotary_dim, interleaved, cos_tab, sin_tab, pos):
+    """Rotate one fp32 vector x at position pos; returns a new fp32 array."""
+    x = np.ascontiguousarray(x, np.float32)
+    c = np.ascontiguousarray(cos_tab, np.float32)
+    s_ = np.ascontiguousarray(sin_tab, np.float32)
+    y = np.zeros_like(x)
+    lib().orc_rotary_f32(_ptr(x), x.size, int(rotary_dim), int(interleaved), _ptr(c), _ptr(s_), int(pos), _ptr(y))
+    return y
+
+
+def append_kv_rotary(p, new_dtype, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens,
+                     cos_tab, sin_tab, rotary_dim, interleaved, q=None):
+    """Returns (k_pages, v_pages, q) copies after the rotary append."""
+    kn, vn = raw(k_new), raw(v_new)
+    k, v = raw(k_pages).copy(), raw(v_pages).copy()
+    ks, vs = raw(k_scale), raw(v_scale)
+    bt, sl = raw(block_table).astype(np.int32), raw(seq_lens).astype(np.int32)
+    c = np.ascontiguousarray(raw(cos_tab), np.float32)
+    s_ = np.ascontiguousarray(raw(sin_tab), np.float32)
+    qq = None if q is None else raw(q).copy()
+    rc = lib().orc_append_kv_rotary(ctypes.byref(p), int(new_dtype), _ptr(kn), _ptr(vn), _ptr(k), _ptr(v), _ptr(ks),
+                                    _ptr(vs), _ptr(bt), _ptr(sl), _ptr(c), _ptr(s_), int(rotary_dim), c.shape[0],
+                                    int(interleaved), _ptr(qq))
+    _check(rc, "append_kv_rotary")
+    return k, v, qq

@@ -22,7 +22,7 @@ FD_DEV_BAD_PAGE, FD_DEV_CAPACITY, FD_DEV_TIMEOUT = 0x1, 0x2, 0x4
 FD_F16, FD_BF16, FD_E4M3, FD_F32 = 0, 1, 2, 3
 
 EXPORTS = ("fd_plan", "fd_decode_paged", "fd_decode_paged_ex", "fd_merge_states", "fd_append_kv",
-           "fd_status_string", "fd_status_from_device", "fd_api_version")
+           "fd_append_kv_rotary", "fd_status_string", "fd_status_from_device", "fd_api_version")
 
 _TORCH_TO_FD = {torch.float16: FD_F16, torch.bfloat16: FD_BF16, torch.float8_e4m3fn: FD_E4M3,
                 torch.float32: FD_F32}
@@ -94,6 +94,8 @@ def load(path: str = LIB_PATH):
     L.fd_merge_states.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
     L.fd_append_kv.restype = I
     L.fd_append_kv.argtypes = [ctypes.POINTER(FdProblem), P, P, P, P, P, P, P, P, P, P]
+    L.fd_append_kv_rotary.restype = I
+    L.fd_append_kv_rotary.argtypes = [ctypes.POINTER(FdProblem), P, P, P, P, P, P, P, P, P, P, I, I, I, P, P, P]
     L.fd_status_string.restype = ctypes.c_char_p
     L.fd_status_string.argtypes = [I]
     L.fd_status_from_device.restype = I
@@ -190,3 +192,16 @@ def fd_append_kv(problem: FdProblem, k_new, v_new, k_pages, v_pages, k_scale, v_
                              _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_append_kv")
+
+
+def fd_append_kv_rotary(problem: FdProblem, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table,
+                        seq_lens, rotary_cos, rotary_sin, interleaved=False, q_inout=None, status=None,
+                        stream=None):
+    """rotary_cos/sin: fp32 [max_pos, rotary_dim/2] on the device."""
+    max_pos, half = rotary_cos.shape
+    rc = load().fd_append_kv_rotary(ctypes.byref(problem), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
+                                    _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
+                                    _ptr(rotary_cos), _ptr(rotary_sin), 2 * half, max_pos, int(bool(interleaved)),
+                                    _ptr(q_inout), _ptr(status), _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_append_kv_rotary")

@@ -503,9 +503,14 @@ fd_status fd_merge_states(const float *o_part, const float *m, const float *d, i
     return launch_merge(mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
-fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void *v_new, void *k_pages,
-                       void *v_pages, const float *k_scale, const float *v_scale, const int32_t *block_table,
-                       const int32_t *seq_lens, int32_t *status_dev, void *stream) {
+}  // extern "C"
+
+namespace {
+
+fd_status append_impl(const fd_problem *problem, const void *k_new, const void *v_new, void *k_pages,
+                      void *v_pages, const float *k_scale, const float *v_scale, const int32_t *block_table,
+                      const int32_t *seq_lens, const float *rotary_cos, const float *rotary_sin, int rotary_dim,
+                      int max_pos, int interleaved, void *q_inout, int32_t *status_dev, void *stream) {
     fd_status st = validate_problem(problem);
     if (st != FD_OK) return st;
     const fd_problem &p = *problem;
@@ -532,7 +537,39 @@ fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void 
     ap.num_pages = p.num_pages;
     ap.kv_kind = p.kv_dtype == FD_F16 ? KV_F16 : (p.kv_dtype == FD_BF16 ? KV_BF16 : KV_E4M3);
     ap.new_is_bf16 = p.q_dtype == FD_BF16 ? 1 : 0;
+    ap.cos = rotary_cos;
+    ap.sin = rotary_sin;
+    ap.rotary_dim = rotary_dim;
+    ap.max_pos = max_pos;
+    ap.interleaved = interleaved ? 1 : 0;
+    ap.q_inout = q_inout;
+    ap.Hq = p.Hq;
+    ap.q_is_bf16 = p.q_dtype == FD_BF16 ? 1 : 0;
     return launch_append(ap, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void *v_new, void *k_pages,
+                       void *v_pages, const float *k_scale, const float *v_scale, const int32_t *block_table,
+                       const int32_t *seq_lens, int32_t *status_dev, void *stream) {
+    return append_impl(problem, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, nullptr,
+                       nullptr, 0, 0, 0, nullptr, status_dev, stream);
+}
+
+fd_status fd_append_kv_rotary(const fd_problem *problem, const void *k_new, const void *v_new, void *k_pages,
+                              void *v_pages, const float *k_scale, const float *v_scale,
+                              const int32_t *block_table, const int32_t *seq_lens, const float *rotary_cos,
+                              const float *rotary_sin, int rotary_dim, int max_pos, int interleaved, void *q_inout,
+                              int32_t *status_dev, void *stream) {
+    if (!problem || !rotary_cos || !rotary_sin || max_pos < 1 || rotary_dim < 2 || (rotary_dim & 1) ||
+        rotary_dim > problem->D || !aligned(rotary_cos, 4) || !aligned(rotary_sin, 4) ||
+        (q_inout && !aligned(q_inout, 4)))
+        return FD_ERR_INVALID_ARG;
+    return append_impl(problem, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, rotary_cos,
+                       rotary_sin, rotary_dim, max_pos, interleaved, q_inout, status_dev, stream);
 }
 
 }  // extern "C"

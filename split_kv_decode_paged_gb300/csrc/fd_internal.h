@@ -73,6 +73,12 @@ struct AppendParams {
     int B, Hkv, D, page_size, max_blocks, num_pages;
     int kv_kind;               // KvKind
     int new_is_bf16;           // for E4M3 caches: input dtype bf16 (1) or f16 (0)
+    // Rotary embedding (cos == null: none): tables [max_pos, rotary_dim/2].
+    const float *cos, *sin;
+    int rotary_dim, max_pos, interleaved;
+    void *q_inout;             // [B, Hq, D] rotated in place, or null
+    int Hq;
+    int q_is_bf16;
 };
 
 // Kernel configuration chosen at plan time.
