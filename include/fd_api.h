@@ -203,6 +203,19 @@ fd_status fd_merge_states(const float *o_part, const float *m, const float *d, i
                           int S, int D, fd_dtype out_dtype, void *out, float *lse,
                           void *stream);
 
+/* Merge two normalised attention states of the same queries over disjoint
+ * token sets (cascade / shared-prefix decode: a state over the shared prefix
+ * and one over each sequence's own suffix) [P2 stage two with d = 1:
+ * m = max(lse_a, lse_b), w = exp(lse - m), out = (w_a out_a + w_b out_b) /
+ * (w_a + w_b), lse = m + ln(w_a + w_b)].
+ *   out_a, out_b  device fp32 [rows, D], 16-byte aligned; lse_a, lse_b fp32 [rows]
+ *   out           device [rows, D] in out_dtype; lse fp32 [rows] or NULL
+ * An empty state has lse = -inf; both empty give out = 0, lse = -inf.
+ * D % 4 == 0. */
+fd_status fd_merge_two(const float *out_a, const float *lse_a, const float *out_b,
+                       const float *lse_b, int rows, int D, fd_dtype out_dtype, void *out,
+                       float *lse, void *stream);
+
 /* Append one token per sequence [P3 §3.2-3.3, §4.2].
  *   k_new, v_new  device [B, Hkv, D] in problem.q_dtype for an FD_E4M3 cache
  *                 (quantised as code = e4m3_rne_satfinite(x / scale[page, kvh]),

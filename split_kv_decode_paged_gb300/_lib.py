@@ -22,7 +22,8 @@ FD_DEV_BAD_PAGE, FD_DEV_CAPACITY, FD_DEV_TIMEOUT = 0x1, 0x2, 0x4
 FD_F16, FD_BF16, FD_E4M3, FD_F32 = 0, 1, 2, 3
 
 EXPORTS = ("fd_plan", "fd_decode_paged", "fd_decode_paged_ex", "fd_merge_states", "fd_append_kv",
-           "fd_append_kv_rotary", "fd_status_string", "fd_status_from_device", "fd_api_version")
+           "fd_append_kv_rotary", "fd_merge_two", "fd_status_string", "fd_status_from_device",
+           "fd_api_version")
 
 _TORCH_TO_FD = {torch.float16: FD_F16, torch.bfloat16: FD_BF16, torch.float8_e4m3fn: FD_E4M3,
                 torch.float32: FD_F32}
@@ -96,6 +97,8 @@ def load(path: str = LIB_PATH):
     L.fd_append_kv.argtypes = [ctypes.POINTER(FdProblem), P, P, P, P, P, P, P, P, P, P]
     L.fd_append_kv_rotary.restype = I
     L.fd_append_kv_rotary.argtypes = [ctypes.POINTER(FdProblem), P, P, P, P, P, P, P, P, P, P, I, I, I, P, P, P]
+    L.fd_merge_two.restype = I
+    L.fd_merge_two.argtypes = [P, P, P, P, I, I, I, P, P, P]
     L.fd_status_string.restype = ctypes.c_char_p
     L.fd_status_string.argtypes = [I]
     L.fd_status_from_device.restype = I
@@ -205,3 +208,13 @@ def fd_append_kv_rotary(problem: FdProblem, k_new, v_new, k_pages, v_pages, k_sc
                                     _ptr(q_inout), _ptr(status), _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_append_kv_rotary")
+
+
+def fd_merge_two(out_a, lse_a, out_b, lse_b, out, lse=None, stream=None):
+    """out_a/out_b fp32 [..., D], lse_a/lse_b fp32 [...] -> out [..., D], lse."""
+    D = out_a.shape[-1]
+    rows = out_a.numel() // D
+    rc = load().fd_merge_two(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), rows, D, fd_dtype(out.dtype),
+                             _ptr(out), _ptr(lse), _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_merge_two")

@@ -552,6 +552,19 @@ fd_status append_impl(const fd_problem *problem, const void *k_new, const void *
 
 extern "C" {
 
+fd_status fd_merge_two(const float *out_a, const float *lse_a, const float *out_b, const float *lse_b, int rows, int D,
+                       fd_dtype out_dtype, void *out, float *lse, void *stream) {
+    if (!out_a || !lse_a || !out_b || !lse_b || !out || rows < 1 || D < 4 || D % 4) return FD_ERR_INVALID_ARG;
+    if (out_dtype != FD_F16 && out_dtype != FD_BF16 && out_dtype != FD_F32) return FD_ERR_UNSUPPORTED;
+    if (!aligned(out_a, 16) || !aligned(out_b, 16) || !aligned(lse_a, 4) || !aligned(lse_b, 4) ||
+        !aligned(out, elem_bytes(out_dtype)) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    return launch_merge_two(out_a, lse_a, out_b, lse_b, rows, D, out_dtype, out, lse,
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FD_OK
+               : FD_ERR_CUDA;
+}
+
 fd_status fd_append_kv(const fd_problem *problem, const void *k_new, const void *v_new, void *k_pages,
                        void *v_pages, const float *k_scale, const float *v_scale, const int32_t *block_table,
                        const int32_t *seq_lens, int32_t *status_dev, void *stream) {

@@ -99,5 +99,7 @@ cudaError_t launch_decode(const fd_problem &p, const KernelShape &ks, const Deco
                           cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &mp, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams &ap, cudaStream_t stream);
+cudaError_t launch_merge_two(const float *oa, const float *la, const float *ob, const float *lb, int rows, int D,
+                             int out_dtype, void *out, float *lse, cudaStream_t stream);
 
 }  // namespace fd

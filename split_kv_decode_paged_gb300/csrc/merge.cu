@@ -80,6 +80,43 @@ __global__ void __launch_bounds__(kMergeThreads) fd_merge_states_kernel(const Me
     }
 }
 
+// Two normalised states (out_a, lse_a) and (out_b, lse_b) of the same query
+// over disjoint token sets: m = max(lse_a, lse_b), w = exp(lse - m),
+// out = (w_a out_a + w_b out_b) / (w_a + w_b), lse = m + ln(w_a + w_b).
+// One thread per (row, 4 elements of D).
+__global__ void fd_merge_two_kernel(const float *oa, const float *la, const float *ob, const float *lb, int rows,
+                                    int D, int out_dtype, void *out, float *lse) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int per_row = D / 4;
+    if (i >= (long long)rows * per_row) return;
+    const long long row = i / per_row;
+    const int d = (int)(i - row * per_row) * 4;
+    const float a = la[row], b = lb[row];
+    const float m = fmaxf(a, b);
+    float wa = 0.f, wb = 0.f;
+    if (m != -INFINITY) {
+        wa = (a == -INFINITY) ? 0.f : __expf(a - m);
+        wb = (b == -INFINITY) ? 0.f : __expf(b - m);
+    }
+    const float den = wa + wb;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float4 va = *reinterpret_cast<const float4 *>(oa + row * D + d);
+    const float4 vb = *reinterpret_cast<const float4 *>(ob + row * D + d);
+    const float r[4] = {(wa * va.x + wb * vb.x) * inv, (wa * va.y + wb * vb.y) * inv, (wa * va.z + wb * vb.z) * inv,
+                        (wa * va.w + wb * vb.w) * inv};
+    for (int k = 0; k < 4; ++k) merge_store(out, row * D + d + k, r[k], out_dtype);
+    if (d == 0 && lse) lse[row] = den > 0.f ? m + logf(den) : -INFINITY;
+}
+
+cudaError_t launch_merge_two(const float *oa, const float *la, const float *ob, const float *lb, int rows, int D,
+                             int out_dtype, void *out, float *lse, cudaStream_t stream) {
+    const long long n = (long long)rows * (D / 4);
+    if (n == 0) return cudaSuccess;
+    fd_merge_two_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(oa, la, ob, lb, rows, D, out_dtype, out,
+                                                                         lse);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_merge(const MergeParams &mp, cudaStream_t stream) {
     if (mp.S > kMergeMaxS || mp.S < 1) return cudaErrorInvalidValue;
     const long long rows = (long long)mp.B * mp.Hq;

@@ -216,3 +216,52 @@ def algorithmic_bytes(spec: Spec, seq_lens, out_bytes_per_elem=None) -> int:
     if spec.kv == "e4m3":
         n += 2 * 4 * spec.Hkv * pages
     return n
+
+
+@dataclass
+class SharedPrefixWorkload:
+    """A batch whose sequences share their first prefix_len tokens (whole
+    pages, stored once) and then continue with their own tokens."""
+    flat: Workload               # per-sequence tables: prefix pages, then own pages
+    prefix_table: torch.Tensor   # [1, prefix_blocks]
+    prefix_len: int
+    suffix_table: torch.Tensor   # [B, suffix_max_blocks]
+    suffix_lens: torch.Tensor    # [B]
+
+
+def make_shared_prefix(spec: Spec, seed: int, prefix_len: int, suffix_lens, device="cpu") -> SharedPrefixWorkload:
+    """Draw a shared-prefix batch: spec gives the shapes and dtypes (its
+    length mix is ignored); the pool holds the prefix pages once."""
+    ps = spec.page_size
+    if prefix_len % ps:
+        raise ValueError("prefix_len must be a multiple of page_size")
+    suffix = torch.as_tensor(suffix_lens, dtype=torch.int32)
+    B = spec.B
+    n_pre = prefix_len // ps
+    n_suf = [(int(L) + ps - 1) // ps for L in suffix.tolist()]
+    flat_lens = suffix + prefix_len
+    # Draw one pool sized for the prefix once plus every suffix, as a flat
+    # workload whose sequence 0 holds the prefix; then rewrite the tables.
+    total_pages = n_pre + sum(n_suf)
+    base = make(Spec(spec.name, B=1, Hq=spec.Hq, Hkv=spec.Hkv, D=spec.D, page_size=ps, kv=spec.kv, q=spec.q,
+                     lens=("list", [total_pages * ps]), pool=("factor", 1.0)), seed, device)
+    pages = base.block_table[0].cpu()
+    prefix_pages = pages[:n_pre]
+    max_suf = max([1] + n_suf)
+    suffix_table = torch.full((B, max_suf), -1, dtype=torch.int32)
+    flat_table = torch.full((B, n_pre + max_suf), -1, dtype=torch.int32)
+    cur = n_pre
+    for b in range(B):
+        own = pages[cur:cur + n_suf[b]]
+        cur += n_suf[b]
+        suffix_table[b, :n_suf[b]] = own
+        flat_table[b, :n_pre] = prefix_pages
+        flat_table[b, n_pre:n_pre + n_suf[b]] = own
+    g = torch.Generator(device=torch.device(device)).manual_seed(int(seed) + 7)
+    q = torch.randn((B, spec.Hq, spec.D), generator=g, dtype=torch.float32, device=device).to(_DT[spec.q])
+    dspec = Spec(spec.name, B=B, Hq=spec.Hq, Hkv=spec.Hkv, D=spec.D, page_size=ps, kv=spec.kv, q=spec.q,
+                 lens=("list", flat_lens.tolist()))
+    flat = Workload(dspec, q, base.k_pages, base.v_pages, base.k_scale, base.v_scale, flat_table.to(device),
+                    flat_lens.to(device), base.num_pages)
+    return SharedPrefixWorkload(flat, prefix_pages.view(1, -1).to(device), prefix_len, suffix_table.to(device),
+                                suffix.to(device))
