@@ -75,8 +75,9 @@ typedef enum { FD_F16 = 0, FD_BF16 = 1, FD_E4M3 = 2, FD_F32 = 3 } fd_dtype;
  *   seq_lens     int32 [B]
  *   out          [B, Hq, D]                      out_dtype (q_dtype or FD_F32)
  *   lse          fp32 [B, Hq], natural log
- * Constraints: Hq % Hkv == 0 and Hq / Hkv <= 16 (query heads of one KV head
- * are the contiguous group hq / (Hq / Hkv) == kvh); D in {64, 128};
+ * Constraints: Hq % Hkv == 0 (the query heads of KV head kvh are the
+ * contiguous group hq / (Hq / Hkv) == kvh; groups larger than 16 heads are
+ * split into 16-head work items); D in {64, 128};
  * page_size % 16 == 0 [P4]; kv_dtype FD_E4M3 requires q_dtype FD_BF16 or
  * FD_F16, otherwise kv_dtype == q_dtype; 1 <= B <= 8192. */
 typedef struct {
@@ -101,6 +102,11 @@ typedef struct {
                            best; 18 reproduces the cookbook's "smallest split
                            count reaching 85% of the best efficiency" [P3 §6.3] */
     int tile_tokens;    /* 0 = default (128); 64 or 128 tokens per pipeline stage */
+    int shared_kv;      /* 1: every q sequence attends the same KV row (one
+                           block-table row, seq_lens[0]; e.g. a shared prefix):
+                           the B*G q rows of each KV head are packed 16 to a
+                           work item so each K/V tile feeds 16 rows; plan with
+                           seq_lens_host[0] = the shared length */
 } fd_plan_options;
 
 /* A plan: plain data in host memory, owned by the caller, reusable for any
@@ -121,7 +127,10 @@ typedef struct {
     size_t ws_partial_md;
     size_t ws_counters;
     long long work_items_hint; /* items for the host lengths (information)      */
-    int reserved[8];
+    int kv_rows;          /* block-table / seq_lens rows the call reads          */
+    int row_fold;         /* q sequences per KV row (1, or B with shared_kv)     */
+    int head_subgroups;   /* work items per (KV row, split, KV head)             */
+    int reserved[5];
 } fd_plan_t;
 
 /* Plan a decode call [P1 §2.1 step 1; P2 进阶突破; P3 §6.3, §8.2].

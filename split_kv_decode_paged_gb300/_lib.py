@@ -51,7 +51,7 @@ class FdProblem(ctypes.Structure):
 class FdPlanOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("num_sms", ctypes.c_int), ("fuse_merge", ctypes.c_int),
                 ("max_seq_len", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("split_margin_pct", ctypes.c_int),
-                ("tile_tokens", ctypes.c_int)]
+                ("tile_tokens", ctypes.c_int), ("shared_kv", ctypes.c_int)]
 
 
 class FdDecodeExtras(ctypes.Structure):
@@ -66,7 +66,8 @@ class FdPlan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
                 ("ws_partial_o", ctypes.c_size_t), ("ws_partial_md", ctypes.c_size_t),
                 ("ws_counters", ctypes.c_size_t), ("work_items_hint", ctypes.c_longlong),
-                ("reserved", ctypes.c_int * 8)]
+                ("kv_rows", ctypes.c_int), ("row_fold", ctypes.c_int), ("head_subgroups", ctypes.c_int),
+                ("reserved", ctypes.c_int * 5)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n not in ("problem", "reserved")}
@@ -142,13 +143,13 @@ def make_problem(B, Hq, Hkv, D, page_size, max_blocks_per_seq, num_pages, q_dtyp
 
 
 def fd_plan(problem: FdProblem, seq_lens_host, num_splits=0, num_sms=0, fuse_merge=1, max_seq_len=0,
-            ctas_per_sm=0, split_margin_pct=0, tile_tokens=0) -> FdPlan:
+            ctas_per_sm=0, split_margin_pct=0, tile_tokens=0, shared_kv=0) -> FdPlan:
     """Plan a decode call; seq_lens_host is a host int32 tensor/sequence."""
     lens = torch.as_tensor(seq_lens_host, dtype=torch.int32).cpu().contiguous()
-    if lens.numel() != problem.B:
+    if lens.numel() != problem.B and not (shared_kv and lens.numel() >= 1):
         raise ValueError("seq_lens_host must have B entries")
     opts = FdPlanOptions(int(num_splits), int(num_sms), int(fuse_merge), int(max_seq_len), int(ctas_per_sm),
-                         int(split_margin_pct), int(tile_tokens))
+                         int(split_margin_pct), int(tile_tokens), int(shared_kv))
     plan = FdPlan()
     rc = load().fd_plan(ctypes.byref(problem), ctypes.c_void_p(lens.data_ptr()), ctypes.byref(opts),
                         ctypes.byref(plan))

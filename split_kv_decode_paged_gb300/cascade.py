@@ -4,10 +4,10 @@ and the two normalised states are merged (vLLM's cascade attention, "FlashAttent
 與 FlashInfer": a shared prefix is computed once; the merge is the
 stage-two rescale formula with d = 1).
 
-All compute runs in libfd: fd_decode_paged_ex (prefix pass: every q row maps
-to the single prefix row through cache_batch_idx, so all of them read the same
-pages), fd_decode_paged (suffix pass) and fd_merge_two.  The prefix must fill
-whole pages.
+All compute runs in libfd.  Prefix pass: fd_decode_paged with a shared_kv
+plan -- the prefix is one KV row and the B*G q rows of each KV head are packed
+16 to a work item, so each prefix tile read feeds 16 query rows.  Suffix pass:
+fd_decode_paged.  Then fd_merge_two.  The prefix must fill whole pages.
 """
 from __future__ import annotations
 
@@ -30,12 +30,11 @@ class CascadeDecoder:
                                         torch.float32)
         self.prob_s = _lib.make_problem(B, Hq, Hkv, D, page_size, suffix_max_blocks, num_pages, q_dtype, kv_dtype,
                                         torch.float32)
-        self.plan_p = _lib.fd_plan(self.prob_p, [prefix_len] * B, **plan_opts)
+        self.plan_p = _lib.fd_plan(self.prob_p, [prefix_len], shared_kv=1, **plan_opts)
         self.plan_s = _lib.fd_plan(self.prob_s, suffix_lens_host, **plan_opts)
         mk = lambda plan: torch.zeros(max(256, plan.workspace_bytes), dtype=torch.uint8, device=self.device)
         self.ws_p, self.ws_s = mk(self.plan_p), mk(self.plan_s)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self.zero_rows = torch.zeros(B, dtype=torch.int32, device=self.device)
         f32 = dict(dtype=torch.float32, device=self.device)
         self.out_p, self.lse_p = torch.empty((B, Hq, D), **f32), torch.empty((B, Hq), **f32)
         self.out_s, self.lse_s = torch.empty((B, Hq, D), **f32), torch.empty((B, Hq), **f32)
@@ -48,9 +47,8 @@ class CascadeDecoder:
             out = torch.empty((self.B, self.Hq, self.D), dtype=q.dtype, device=q.device)
         if lse is None:
             lse = torch.empty((self.B, self.Hq), dtype=torch.float32, device=q.device)
-        _lib.fd_decode_paged_ex(self.plan_p, q, k_pages, v_pages, k_scale, v_scale, prefix_table, prefix_len_dev,
-                                self.out_p, self.lse_p, self.ws_p, cache_batch_idx=self.zero_rows, cache_rows=1,
-                                status=self.status, stream=stream)
+        _lib.fd_decode_paged(self.plan_p, q, k_pages, v_pages, k_scale, v_scale, prefix_table, prefix_len_dev,
+                             self.out_p, self.lse_p, self.ws_p, self.status, stream)
         _lib.fd_decode_paged(self.plan_s, q, k_pages, v_pages, k_scale, v_scale, suffix_table, suffix_lens,
                              self.out_s, self.lse_s, self.ws_s, self.status, stream)
         _lib.fd_merge_two(self.out_p, self.lse_p, self.out_s, self.lse_s, out, lse, stream)

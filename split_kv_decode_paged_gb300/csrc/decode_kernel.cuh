@@ -45,7 +45,8 @@ constexpr int kFlagLast = 2;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct StageMeta {
-    int b, kvh, s, t0, nvalid, flags, nsplit, vlo;  // valid tile rows: [vlo, nvalid)
+    int b, kvh, s, t0, nvalid, flags, nsplit, vlo;  // b: KV row; valid tile rows [vlo, nvalid)
+    int hg, nrows;                                  // head sub-group and its number of q rows
     float kscale[kMaxBoxesPerTile];
     float vscale[kMaxBoxesPerTile];
 };
@@ -117,14 +118,22 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
         reinterpret_cast<float *>(out)[idx] = v;
 }
 
-// Fused merge of the nsplit partial states of (b, kvh), run by the consumer
-// warps of the CTA that completed the last split.  alpha: >= G*nsplit floats.
+// Global q row (b * Hq + hq) of row j of head sub-group hg of (KV row bkv, kvh).
+__device__ __forceinline__ size_t q_row(const DecodeParams &p, int bkv, int kvh, int hg, int j, int qrows) {
+    const int i = hg * qrows + j;
+    const int bq = bkv * p.fold + i / p.G;
+    return (size_t)bq * p.Hq + (size_t)kvh * p.G + (i % p.G);
+}
+
+// Fused merge of the nsplit partial states of the nrows q rows of one
+// (KV row, kvh, head sub-group), run by the consumer warps of the CTA that
+// completed the last split.  alpha: >= nrows*nsplit floats.
 template <int NC>
-__device__ void merge_group(const DecodeParams &p, int b, int kvh, int nsplit, float *alpha, int warp,
-                            int lane, int D) {
-    const int G = p.G, S = p.S;
-    for (int h = warp; h < G; h += NC) {
-        const size_t row = (size_t)b * p.Hq + (size_t)kvh * G + h;
+__device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int nrows, int qrows, int nsplit,
+                            float *alpha, int warp, int lane, int D) {
+    const int S = p.S;
+    for (int h = warp; h < nrows; h += NC) {
+        const size_t row = q_row(p, b, kvh, hg, h, qrows);
         const float *pm = p.part_m + row * S;
         const float *pd = p.part_d + row * S;
         float mx = -INFINITY;
@@ -147,9 +156,9 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int nsplit, f
     }
     named_bar_sync(1, NC * 32);
     const int tid = warp * 32 + lane;
-    for (int idx = tid; idx < G * D; idx += NC * 32) {
+    for (int idx = tid; idx < nrows * D; idx += NC * 32) {
         const int h = idx / D, d = idx - h * D;
-        const size_t row = (size_t)b * p.Hq + (size_t)kvh * G + h;
+        const size_t row = q_row(p, b, kvh, hg, h, qrows);
         const float *po = p.part_o + row * S * D + d;
         float acc = 0.f;
         for (int s = 0; s < nsplit; ++s) acc += alpha[h * nsplit + s] * ldcg(po + (size_t)s * D);
@@ -204,7 +213,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 
     if (warp == NC) {
         // ================================================================ producer
-        const int B = p.B, Hkv = p.Hkv, C = p.chunk, ps = p.page_size, boxr = p.boxr;
+        const int B = p.Bkv, Hkv = p.Hkv, C = p.chunk, ps = p.page_size, boxr = p.boxr;
+        const int NHG = p.nhg, HG = Hkv * p.nhg;  // items per chunk of a KV row
         // K/V are streamed once per call: keep them from displacing other lines in L2.
         const uint64_t kv_policy = l2_policy_evict_first();
         const int BPT = TILE / boxr;  // boxes per tile: 1, 2, 4 (or 8)
@@ -286,7 +296,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             int v = 0;
             if (i < B) {
                 const int L = lens[order[i]];
-                v = (L == 0 ? 1 : (L + C - 1) / C) * Hkv;
+                v = (L == 0 ? 1 : (L + C - 1) / C) * HG;
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // Tokens [t_begin, t_end) of cache row cb; tiles start at the box
         // boundary a <= t_begin, and the first tile masks its vlo leading rows.
         struct Item {
-            int b, cb, s, kvh, L, nsplit, t_begin, t_end, ntok, ntiles, nbox, box0, vlo;
+            int b, cb, s, kvh, hg, nrows, L, nsplit, t_begin, t_end, ntok, ntiles, nbox, box0, vlo;
         };
         auto decode_item = [&](int item) -> Item {
             int lo = 0, hi = B - 1;
@@ -314,11 +324,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
             Item it;
             it.b = order[lo];
+            // within a KV row: split-major, then kvh, then head sub-group (the
+            // sub-groups of one (split, kvh) read the same K/V back to back)
             const int rem = item - prefix[lo];
-            it.s = rem / Hkv;
-            it.kvh = rem - it.s * Hkv;
+            it.s = rem / HG;
+            const int r2 = rem - it.s * HG;
+            it.kvh = r2 / NHG;
+            it.hg = r2 - it.kvh * NHG;
+            it.nrows = min(QROWS, p.G * p.fold - it.hg * QROWS);
             it.L = lens[it.b];
-            it.nsplit = (prefix[lo + 1] - prefix[lo]) / Hkv;
+            it.nsplit = (prefix[lo + 1] - prefix[lo]) / HG;
             it.cb = it.b;
             int lp = 0;
             if (p.batch_idx) {
@@ -421,12 +436,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 const int t0 = t_begin + j * TILE;
                 const bool load_q = (j == 0) && (ntok > 0);
                 const uint32_t bytes = (uint32_t)__popc(good_mask) * 2u * (uint32_t)(boxr * Sh::RB) +
-                                       (load_q ? (uint32_t)(p.G * D * 2) : 0u);
+                                       (load_q ? (uint32_t)(cur.nrows * D * 2) : 0u);
                 StageMeta *m = &meta[st];
                 if (lane == 0) {
                     m->b = b; m->kvh = kvh; m->s = s; m->t0 = t0;
                     m->nvalid = max(0, min(TILE, t_end - t0));
                     m->vlo = j == 0 ? cur.vlo : 0;
+                    m->hg = cur.hg;
+                    m->nrows = cur.nrows;
                     m->flags = (j == 0 ? kFlagFirst : 0) | (j == ntiles - 1 ? kFlagLast : 0);
                     m->nsplit = nsplit;
                 }
@@ -441,10 +458,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
                 __syncwarp();
                 uint8_t *sb = stages + (size_t)st * Sh::STAGE;
-                if (load_q && lane == 0) {
-                    const uint8_t *qsrc = reinterpret_cast<const uint8_t *>(p.q) +
-                                          ((size_t)b * p.Hq + (size_t)kvh * p.G) * D * 2;
-                    bulk_load(smem_u32(sb + 2 * Sh::KV_REGION), qsrc, (uint32_t)(p.G * D * 2), fb);
+                if (load_q) {
+                    // The item's q rows: one contiguous run of heads per q
+                    // sequence it spans; lane t copies run t.
+                    const int i0 = cur.hg * QROWS, i1 = i0 + cur.nrows, Gh = p.G;
+                    const int bq0 = i0 / Gh;
+                    const int ia = max(i0, (bq0 + lane) * Gh), ib = min(i1, (bq0 + lane + 1) * Gh);
+                    if (ia < ib) {
+                        const int bq = b * p.fold + ia / Gh;
+                        const uint8_t *qsrc = reinterpret_cast<const uint8_t *>(p.q) +
+                                              ((size_t)bq * p.Hq + (size_t)kvh * Gh + (ia % Gh)) * D * 2;
+                        bulk_load(smem_u32(sb + 2 * Sh::KV_REGION + (ia - i0) * D * 2), qsrc,
+                                  (uint32_t)((ib - ia) * D * 2), fb);
+                    }
                 }
                 if (good) {
                     // One box = boxr token rows x the whole D of one KV head,
@@ -519,7 +545,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             // Query fragments (B operand of QK), zero for padded heads.
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const bool live_head = (n * 8 + g) < p.G;
+                const bool live_head = (n * 8 + g) < mt.nrows;
                 if constexpr (!FP8) {
 #pragma unroll
                     for (int kk = 0; kk < KT; kk += 2) {
@@ -764,7 +790,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         }  // sub-tiles
         // Release the stage (all reads of it are done).
-        const int m_kvh = mt.kvh, m_s = mt.s, m_nsplit = mt.nsplit;
+        const int m_kvh = mt.kvh, m_s = mt.s, m_nsplit = mt.nsplit, m_hg = mt.hg, m_nrows = mt.nrows;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
         if (++st == NST) { st = 0; ph ^= 1u; }
@@ -807,7 +833,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         named_bar_sync(1, NC * 32);
         const int tid = warp * 32 + lane;
-        const int G = p.G;
+        const int G = m_nrows;  // q rows of this item
         // Per head: combined max, the warps' weights (in place of their max)
         // and the combined denominator; then the D outputs in float4 groups.
         if (tid < G) {
@@ -823,7 +849,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 Ls += a * scr_l[w * QROWS + h];
             }
             const bool empty = !(Ls > 0.f);
-            const size_t row = (size_t)mb * p.Hq + (size_t)m_kvh * G + h;
+            const size_t row = q_row(p, mb, m_kvh, m_hg, h, QROWS);
             if (m_nsplit == 1) {
                 scr_inv[h] = empty ? 0.f : 1.f / Ls;
                 if (p.lse) p.lse[row] = empty ? -INFINITY : (M + __log2f(Ls)) * kLn2;
@@ -846,7 +872,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 acc.z = fmaf(a, v.z, acc.z);
                 acc.w = fmaf(a, v.w, acc.w);
             }
-            const size_t row = (size_t)mb * p.Hq + (size_t)m_kvh * G + h;
+            const size_t row = q_row(p, mb, m_kvh, m_hg, h, QROWS);
             if (m_nsplit == 1) {
                 const float inv = scr_inv[h];
                 store_out4(p.out, row * D + d, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.out_dtype);
@@ -862,14 +888,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             named_bar_sync(1, NC * 32);
             if (tid == 0) {
                 __threadfence();
-                const int prev = atomicAdd(p.merge_ctr + (size_t)mb * p.Hkv + m_kvh, 1);
+                const int prev = atomicAdd(p.merge_ctr + ((size_t)mb * p.Hkv + m_kvh) * p.nhg + m_hg, 1);
                 __threadfence();
                 *scr_flag = (prev == m_nsplit - 1);
             }
             named_bar_sync(1, NC * 32);
             if (*scr_flag) {
-                merge_group<NC>(p, mb, m_kvh, m_nsplit, scratch, warp, lane, D);
-                if (tid == 0) atomicExch(p.merge_ctr + (size_t)mb * p.Hkv + m_kvh, 0);
+                merge_group<NC>(p, mb, m_kvh, m_hg, m_nrows, QROWS, m_nsplit, scratch, warp, lane, D);
+                if (tid == 0) atomicExch(p.merge_ctr + ((size_t)mb * p.Hkv + m_kvh) * p.nhg + m_hg, 0);
             }
         }
         named_bar_sync(1, NC * 32);

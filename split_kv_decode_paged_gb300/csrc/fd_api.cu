@@ -23,7 +23,7 @@ size_t decode_smem_f16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
 
-KernelShape kernel_shape(const fd_problem &p, int tile_tokens) {
+KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold) {
     KernelShape ks;
     const int tile = tile_tokens == 64 ? 64 : 128;
     if (tile == 64) {
@@ -37,7 +37,7 @@ KernelShape kernel_shape(const fd_problem &p, int tile_tokens) {
         ks.subtiles = 2;
     }
     ks.tile = ks.consumer_warps * ks.subtiles * kTokensPerWarp;
-    ks.nt = (p.Hq / p.Hkv) <= 8 ? 1 : 2;
+    ks.nt = (p.Hq / p.Hkv) * fold <= 8 ? 1 : 2;
     return ks;
 }
 
@@ -94,7 +94,6 @@ fd_status validate_problem(const fd_problem *p) {
     }
     if (p->out_dtype != p->q_dtype && p->out_dtype != FD_F32) return FD_ERR_UNSUPPORTED;
     if (p->D != 64 && p->D != 128) return FD_ERR_UNSUPPORTED;
-    if (p->Hq / p->Hkv > 16) return FD_ERR_UNSUPPORTED;
     if (p->B > kMaxBatch) return FD_ERR_UNSUPPORTED;
     if ((long long)p->page_size * p->max_blocks_per_seq > (1LL << 30)) return FD_ERR_UNSUPPORTED;
     return FD_OK;
@@ -266,17 +265,21 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (!plan || !seq_lens_host) return FD_ERR_INVALID_ARG;
     fd_status st = validate_problem(problem);
     if (st != FD_OK) return st;
-    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0};
+    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0, 0};
     if (options) opt = *options;
     if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 ||
         opt.split_margin_pct < 0 || opt.split_margin_pct > 100 ||
         (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128))
         return FD_ERR_INVALID_ARG;
+    // shared_kv: every q sequence attends KV row 0 (one block-table row, one
+    // seq_lens entry): the B*G q rows of a KV head are sliced into items.
+    const int fold = opt.shared_kv ? problem->B : 1;
+    const int kv_rows = opt.shared_kv ? 1 : problem->B;
     const double margin = (opt.split_margin_pct > 0 ? opt.split_margin_pct : kDefaultSplitMarginPct) / 100.0;
     const fd_problem &p = *problem;
-    std::vector<int> lens(p.B);
+    std::vector<int> lens(kv_rows);
     long long maxL = 0;
-    for (int b = 0; b < p.B; ++b) {
+    for (int b = 0; b < kv_rows; ++b) {
         if (seq_lens_host[b] < 0) return FD_ERR_INVALID_ARG;
         lens[b] = seq_lens_host[b];
         maxL = std::max<long long>(maxL, lens[b]);
@@ -295,8 +298,13 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         if (st != FD_OK) return st;
         sms = di.sms;
     }
-    const KernelShape ks = kernel_shape(p, opt.tile_tokens);
+    const KernelShape ks = kernel_shape(p, opt.tile_tokens, fold);
     const int tile = ks.tile;
+    const int qrows = 8 * ks.nt;
+    const int nhg = ((p.Hq / p.Hkv) * fold + qrows - 1) / qrows;
+    fd_problem pk = p;  // the KV side of the problem: kv_rows rows, nhg items per KV head
+    pk.B = kv_rows;
+    pk.Hkv = p.Hkv * nhg;
     const int ctas_per_sm = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
     const int P = sms * ctas_per_sm;
 
@@ -305,7 +313,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         const int S = std::min(opt.num_splits, kMaxSplits);
         C = std::max(tile, round_up((std::max<long long>(maxL, 1) + S - 1) / S, tile));
     } else {
-        C = choose_chunk(lens, p, P, tile, margin);
+        C = choose_chunk(lens, pk, P, tile, margin);
     }
     int slots = (int)std::max<long long>(1, (capL + C - 1) / C);
     if (slots > kMaxSplits) {
@@ -313,7 +321,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         slots = (int)std::max<long long>(1, (capL + C - 1) / C);
     }
     long long items = 0;
-    for (int L : lens) items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv;
+    for (int L : lens) items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv * nhg;
 
     // Deepest pipeline that fits in shared memory.
     int stages = 0;
@@ -340,6 +348,9 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     plan->stages = stages;
     plan->smem_bytes = (int)smem;
     plan->work_items_hint = items;
+    plan->kv_rows = kv_rows;
+    plan->row_fold = fold;
+    plan->head_subgroups = nhg;
     const size_t rows = (size_t)p.B * p.Hq;
     size_t off = 0;
     plan->ws_partial_o = off;
@@ -347,7 +358,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     plan->ws_partial_md = off;
     off += align256(slots > 1 ? 2 * rows * slots * sizeof(float) : 0);
     plan->ws_counters = off;
-    off += align256(((size_t)p.B * p.Hkv + 2) * sizeof(int));
+    off += align256(((size_t)kv_rows * p.Hkv * nhg + 2) * sizeof(int));
     plan->workspace_bytes = off;
     return FD_OK;
 }
@@ -372,7 +383,11 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
         (v_scale && !aligned(v_scale, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return FD_ERR_INVALID_ARG;
     if (workspace_bytes < plan->workspace_bytes) return FD_ERR_WORKSPACE_TOO_SMALL;
-    const KernelShape ks = kernel_shape(p, plan->tile_tokens);
+    const int fold = plan->row_fold;
+    if (fold < 1 || plan->kv_rows < 1 || plan->kv_rows * fold != p.B || plan->head_subgroups < 1) return FD_ERR_INVALID_ARG;
+    if (fold > 1 && ex && (ex->cache_batch_idx || ex->cache_leftpad)) return FD_ERR_UNSUPPORTED;
+    const KernelShape ks = kernel_shape(p, plan->tile_tokens, fold);
+    if (plan->head_subgroups != ((p.Hq / p.Hkv) * fold + 8 * ks.nt - 1) / (8 * ks.nt)) return FD_ERR_INVALID_ARG;
     if (plan->tile_tokens != ks.tile || plan->chunk_tokens < ks.tile || plan->chunk_tokens % ks.tile != 0 ||
         plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->stages < kMinStages ||
         plan->stages > kMaxStages || plan->grid_ctas < 1)
@@ -391,7 +406,7 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     dp.seq_lens = seq_lens;
     dp.batch_idx = ex ? ex->cache_batch_idx : nullptr;
     dp.leftpad = ex ? ex->cache_leftpad : nullptr;
-    dp.cache_rows = (ex && ex->cache_batch_idx) ? ex->cache_rows : p.B;
+    dp.cache_rows = (ex && ex->cache_batch_idx) ? ex->cache_rows : plan->kv_rows;
     dp.k_scale = k_scale;
     dp.v_scale = v_scale;
     dp.out = out;
@@ -401,13 +416,16 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     dp.part_d = dp.part_m + rows * plan->num_splits;
     int *ctr = reinterpret_cast<int *>(ws + plan->ws_counters);
     dp.merge_ctr = ctr;
-    dp.work_ctr = ctr + (size_t)p.B * p.Hkv;
+    dp.work_ctr = ctr + (size_t)plan->kv_rows * p.Hkv * plan->head_subgroups;
     dp.done_ctr = dp.work_ctr + 1;
     dp.status = status_dev;
     dp.B = p.B;
     dp.Hq = p.Hq;
     dp.Hkv = p.Hkv;
     dp.G = p.Hq / p.Hkv;
+    dp.fold = fold;
+    dp.nhg = plan->head_subgroups;
+    dp.Bkv = plan->kv_rows;
     dp.page_size = p.page_size;
     dp.max_blocks = p.max_blocks_per_seq;
     dp.num_pages = p.num_pages;
@@ -441,6 +459,7 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
         mp.D = p.D;
         mp.chunk = plan->chunk_tokens;
         mp.cap = dp.cap;
+        mp.fold = fold;
         mp.out_dtype = p.out_dtype;
         e = launch_merge(mp, s);
         if (e != cudaSuccess) return FD_ERR_CUDA;
@@ -499,6 +518,7 @@ fd_status fd_merge_states(const float *o_part, const float *m, const float *d, i
     mp.D = D;
     mp.chunk = 1;
     mp.cap = 0;
+    mp.fold = 1;
     mp.out_dtype = out_dtype;
     return launch_merge(mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }

@@ -40,6 +40,11 @@ struct DecodeParams {
     int *done_ctr;             // 1
     int *status;               // null allowed
     int B, Hq, Hkv, G;
+    // Query rows of one work item: the G*fold rows that read KV head kvh of
+    // KV row bkv (fold > 1: several q sequences share one KV row), sliced
+    // into nhg sub-groups of at most 8*NT rows.  Row i of the group is q
+    // sequence bkv*fold + i/G, head kvh*G + i%G.
+    int fold, nhg, Bkv;
     int page_size, max_blocks, num_pages;
     int S;                     // partial slots per (b, hq)
     int chunk;                 // tokens per split
@@ -61,6 +66,7 @@ struct MergeParams {
     const int32_t *leftpad;
     int cache_rows;
     int B, Hq, S, D, chunk, cap;
+    int fold;                  // q sequences per KV row
     int out_dtype;
 };
 
@@ -89,8 +95,9 @@ struct KernelShape {
     int nt;              // 8-wide head tiles: 1 (G <= 8) or 2 (G <= 16)
 };
 
-// tile_tokens: 64 or 128 (0 = default for the K/V type).
-KernelShape kernel_shape(const fd_problem &p, int tile_tokens);
+// tile_tokens: 64 or 128 (0 = default for the K/V type); fold: q sequences
+// per KV row (1 = ordinary decode).
+KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold);
 size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages);
 int decode_max_stages(const fd_problem &p, const KernelShape &ks);
 

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kMergeThreads) fd_merge_states_kernel(const Me
     if (p.seq_lens) {
         // Rows of sequences that were not split were written by the decode
         // kernel itself; only the split ones are merged here.
-        int cb = b;
+        int cb = b / p.fold;  // KV row of this q sequence
         if (p.batch_idx) {
             cb = p.batch_idx[b];
             if (cb < 0 || cb >= p.cache_rows) return;

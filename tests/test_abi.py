@@ -51,7 +51,6 @@ def _prob(**kw):
     (dict(page_size=24), _lib.FD_ERR_INVALID_ARG),          # not a multiple of 16
     (dict(Hq=6, Hkv=4), _lib.FD_ERR_INVALID_ARG),           # Hq % Hkv != 0
     (dict(D=96), _lib.FD_ERR_UNSUPPORTED),
-    (dict(Hq=34, Hkv=2), _lib.FD_ERR_UNSUPPORTED),          # group of 17 heads
     (dict(q_dtype=torch.float16), _lib.FD_ERR_UNSUPPORTED),  # q/kv mismatch without fp8
     (dict(B=0), _lib.FD_ERR_INVALID_ARG),
     (dict(B=9000), _lib.FD_ERR_UNSUPPORTED),

@@ -50,6 +50,10 @@ SMALL = [
     ("fp8 bf16q d64 g1", 2, 2, 2, 64, 64, "e4m3", "bf16", [70, 9]),
     ("fp8 bf16q g16", 1, 32, 2, 128, 128, "e4m3", "bf16", [700]),
     ("empty and one token", 3, 8, 2, 128, 16, "bf16", "bf16", [0, 1, 17]),
+    ("gqa bf16 g20 (two head sub-groups)", 2, 40, 2, 128, 16, "bf16", "bf16", [90, 700]),
+    ("gqa bf16 g32", 2, 64, 2, 128, 64, "bf16", "bf16", [300, 1200]),
+    ("mqa f16 g48 d64", 1, 48, 1, 64, 16, "f16", "f16", [517]),
+    ("fp8 g32", 2, 64, 2, 128, 128, "e4m3", "bf16", [200, 900]),
 ]
 
 

@@ -83,3 +83,16 @@ def test_plan_invariants(fdlib):
         plan2 = _lib.fd_plan(prob, lens, num_sms=148, max_seq_len=int(lens.max()) + 1000) \
             if int(lens.max()) + 1000 <= spec.page_size * mb else plan
         assert plan2.capacity_tokens >= plan.capacity_tokens
+
+
+def test_head_subgroups_and_shared_kv(fdlib):
+    # groups above 16 heads are sliced into 16-row items
+    prob = _lib.make_problem(2, 64, 2, 128, 16, 64, 200, torch.bfloat16, torch.bfloat16)
+    plan = _lib.fd_plan(prob, [1000, 1000], num_sms=148, num_splits=1)
+    assert plan.head_subgroups == 2 and plan.row_fold == 1 and plan.kv_rows == 2
+    assert plan.work_items_hint == 2 * 2 * 2
+    # shared KV: 64 q sequences x 4 heads per KV head -> 16 items per (chunk, kvh)
+    prob = _lib.make_problem(64, 32, 8, 128, 16, 256, 300, torch.bfloat16, torch.bfloat16)
+    plan = _lib.fd_plan(prob, [4096], num_sms=148, shared_kv=1, num_splits=1)
+    assert plan.row_fold == 64 and plan.kv_rows == 1 and plan.head_subgroups == 16
+    assert plan.work_items_hint == 8 * 16
