@@ -39,7 +39,7 @@
 
 namespace fd {
 
-constexpr int kOrderBuckets = 64;  // length buckets of the longest-first dispatch order (2 per lane)
+constexpr int kOrderBuckets = 64;  // length buckets of the partial-chunk dispatch order (2 per lane)
 constexpr int kFlagFirst = 1;
 constexpr int kFlagLast = 2;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -155,14 +155,31 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int n
         if (lane == 0 && p.lse) p.lse[row] = empty ? -INFINITY : mx + logf(sum);
     }
     named_bar_sync(1, NC * 32);
+    // Outputs in float4 groups; the split loop issues 8 independent L2 loads
+    // per batch so the merge is not one load latency per split.
     const int tid = warp * 32 + lane;
-    for (int idx = tid; idx < nrows * D; idx += NC * 32) {
-        const int h = idx / D, d = idx - h * D;
+    for (int idx = tid; idx < nrows * (D / 4); idx += NC * 32) {
+        const int h = idx / (D / 4), d = (idx - h * (D / 4)) * 4;
         const size_t row = q_row(p, b, kvh, hg, h, qrows);
         const float *po = p.part_o + row * S * D + d;
-        float acc = 0.f;
-        for (int s = 0; s < nsplit; ++s) acc += alpha[h * nsplit + s] * ldcg(po + (size_t)s * D);
-        store_out(p.out, row * D + d, acc, p.out_dtype);
+        const float *al = alpha + h * nsplit;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < nsplit; s0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                v[k] = (s0 + k < nsplit) ? __ldcg(reinterpret_cast<const float4 *>(po + (size_t)(s0 + k) * D))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float a = (s0 + k < nsplit) ? al[s0 + k] : 0.f;
+                acc.x = fmaf(a, v[k].x, acc.x);
+                acc.y = fmaf(a, v[k].y, acc.y);
+                acc.z = fmaf(a, v[k].z, acc.z);
+                acc.w = fmaf(a, v[k].w, acc.w);
+            }
+        }
+        store_out4(p.out, row * D + d, acc.x, acc.y, acc.z, acc.w, p.out_dtype);
     }
 }
 
@@ -229,16 +246,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
             return cb;
         };
-        // Dispatch order: sequences sorted longest first into kOrderBuckets
-        // length buckets (stable, identical in every CTA because it depends
-        // only on seq_lens), so the short items come last and fill the tail.
-        // Then the item counts in that order and their prefix sums.
+        // Dispatch order, identical in every CTA (it depends only on seq_lens):
+        //  A: every full chunk (C tokens) of every KV row, in row order;
+        //  B: the last, partial chunk of each row (or the single empty item of
+        //     an empty row), rows sorted by that chunk's length, longest first
+        //     (stable counting sort into kOrderBuckets buckets).
+        // Largest items go first and the smallest fill the tail.
         for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
         __syncwarp();
-        const long long cap1 = (long long)p.cap + 1;
+        const long long c1 = (long long)C + 1;
+        auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
+        auto bucket_of = [&](int r) {
+            return (kOrderBuckets - 1) - (int)min((long long)(kOrderBuckets - 1), ((long long)r * kOrderBuckets) / c1);
+        };
+        int runningA = 0;
         for (int base = 0; base < B; base += 32) {
             const int b = base + lane;
-            int bucket = kOrderBuckets;  // sentinel for lanes past B
+            int bucket = kOrderBuckets;  // sentinel: past B or no partial chunk
+            int vA = 0;
             if (b < B) {
                 // Attended length: tokens [leftpad, seq_len) of the q row's cache row.
                 const int cb = cache_row(b);
@@ -255,12 +280,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     L = L < 0 ? 0 : p.cap;
                 }
                 lens[b] = L;
-                bucket = (kOrderBuckets - 1) - (int)min((long long)(kOrderBuckets - 1), (L * (long long)kOrderBuckets) / cap1);
+                vA = (L / C) * HG;
+                const int r = tail_of(L);
+                if (r >= 0) bucket = bucket_of(r);
             }
             const unsigned peers = __match_any_sync(0xffffffffu, bucket);
-            if (b < B && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+            if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, vA, o);
+                if (lane >= o) vA += t;
+            }
+            if (b < B) prefix[b + 1] = runningA + vA;
+            runningA += __shfl_sync(0xffffffffu, vA, 31);
             __syncwarp();
         }
+        if (lane == 0) prefix[0] = 0;
+        int nB = 0;
         {   // exclusive scan of the bucket counts (2 buckets per lane)
             const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
             int v = h0 + h1;
@@ -269,6 +305,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 const int t = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += t;
             }
+            nB = __shfl_sync(0xffffffffu, v, 31);
             const int excl = v - h0 - h1;
             __syncwarp();
             hist[2 * lane] = excl;
@@ -277,38 +314,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         for (int base = 0; base < B; base += 32) {
             const int b = base + lane;
-            const int L = b < B ? lens[b] : 0;
-            const int bucket = b < B ? (kOrderBuckets - 1) - (int)min((long long)(kOrderBuckets - 1),
-                                                                  (L * (long long)kOrderBuckets) / cap1)
-                                     : kOrderBuckets;
+            const int r = b < B ? tail_of(lens[b]) : -1;
+            const int bucket = r >= 0 ? bucket_of(r) : kOrderBuckets;
             const unsigned peers = __match_any_sync(0xffffffffu, bucket);
-            if (b < B) {
+            if (bucket < kOrderBuckets) {
                 const unsigned below = peers & ((1u << lane) - 1u);
                 order[hist[bucket] + __popc(below)] = b;
             }
             __syncwarp();
-            if (b < B && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+            if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
             __syncwarp();
         }
-        int running = 0;
-        for (int base = 0; base < B; base += 32) {
-            const int i = base + lane;
-            int v = 0;
-            if (i < B) {
-                const int L = lens[order[i]];
-                v = (L == 0 ? 1 : (L + C - 1) / C) * HG;
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += t;
-            }
-            if (i < B) prefix[i + 1] = running + v;
-            running += __shfl_sync(0xffffffffu, v, 31);
-        }
-        if (lane == 0) prefix[0] = 0;
-        __syncwarp();
-        const int total = running;
+        const int totalA = runningA;
+        const int total = totalA + nB * HG;
 
         // Item -> (b, split, kvh) and its token range.
         // Tokens [t_begin, t_end) of cache row cb; tiles start at the box
@@ -317,23 +335,31 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             int b, cb, s, kvh, hg, nrows, L, nsplit, t_begin, t_end, ntok, ntiles, nbox, box0, vlo;
         };
         auto decode_item = [&](int item) -> Item {
-            int lo = 0, hi = B - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
-            }
             Item it;
-            it.b = order[lo];
-            // within a KV row: split-major, then kvh, then head sub-group (the
-            // sub-groups of one (split, kvh) read the same K/V back to back)
-            const int rem = item - prefix[lo];
-            it.s = rem / HG;
-            const int r2 = rem - it.s * HG;
+            int r2;
+            if (item < totalA) {
+                int lo = 0, hi = B - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+                }
+                it.b = lo;
+                // within a KV row: split-major, then kvh, then head sub-group
+                // (the sub-groups of one (split, kvh) read the same K/V back to back)
+                const int rem = item - prefix[lo];
+                it.s = rem / HG;
+                r2 = rem - it.s * HG;
+            } else {
+                const int k = (item - totalA) / HG;
+                it.b = order[k];
+                it.s = lens[it.b] / C;
+                r2 = (item - totalA) - k * HG;
+            }
             it.kvh = r2 / NHG;
             it.hg = r2 - it.kvh * NHG;
             it.nrows = min(QROWS, p.G * p.fold - it.hg * QROWS);
             it.L = lens[it.b];
-            it.nsplit = (prefix[lo + 1] - prefix[lo]) / HG;
+            it.nsplit = it.L == 0 ? 1 : (it.L + C - 1) / C;
             it.cb = it.b;
             int lp = 0;
             if (p.batch_idx) {

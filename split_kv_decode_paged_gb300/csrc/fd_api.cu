@@ -126,24 +126,27 @@ int round_up(long long x, int a) { return (int)(((x + a - 1) / a) * a); }
 
 // Greedy list-scheduling estimate of the busiest CTA (in token-times) when
 // the items of chunk length C are handed out to P CTAs in the kernel's
-// dispatch order (sequences longest first, then split, then KV head).
-double makespan(const std::vector<int> &lens_in, int Hkv, int C, int P, double item_ovh) {
-    std::vector<int> lens(lens_in);
-    std::stable_sort(lens.begin(), lens.end(), [](int a, int b) { return a > b; });
+// dispatch order: every full chunk first, then each sequence's partial
+// chunk, longest first (Hkv items per chunk).
+double makespan(const std::vector<int> &lens, int Hkv, int C, int P, double item_ovh) {
+    std::vector<int> items;
+    std::vector<int> tails;
+    for (int L : lens) {
+        for (int s = 0; s < L / C; ++s) items.push_back(C);
+        if (L == 0 || L % C) tails.push_back(L % C);
+    }
+    std::stable_sort(tails.begin(), tails.end(), [](int a, int b) { return a > b; });
+    items.insert(items.end(), tails.begin(), tails.end());
     std::priority_queue<double, std::vector<double>, std::greater<double>> q;
     for (int i = 0; i < P; ++i) q.push(0.0);
     double worst = 0.0;
-    for (int L : lens) {
-        const int n = L == 0 ? 1 : (L + C - 1) / C;
-        for (int s = 0; s < n; ++s) {
-            const int len = std::max(0, std::min(C, L - s * C));
-            for (int h = 0; h < Hkv; ++h) {
-                double t = q.top();
-                q.pop();
-                t += len + item_ovh;
-                worst = std::max(worst, t);
-                q.push(t);
-            }
+    for (int len : items) {
+        for (int h = 0; h < Hkv; ++h) {
+            double t = q.top();
+            q.pop();
+            t += len + item_ovh;
+            worst = std::max(worst, t);
+            q.push(t);
         }
     }
     return worst;

@@ -73,9 +73,16 @@ __global__ void __launch_bounds__(kMergeThreads) fd_merge_states_kernel(const Me
     const float inv = s_inv;
     if (threadIdx.x == 0 && p.lse) p.lse[row] = s_lse_m;
     const float *po = p.part_o + row * (size_t)p.S * p.D;
+    // 8 independent loads in flight per batch of splits.
     for (int d = threadIdx.x; d < p.D; d += kMergeThreads) {
         float acc = 0.f;
-        for (int s = 0; s < n; ++s) acc += w[s] * po[(size_t)s * p.D + d];
+        for (int s0 = 0; s0 < n; s0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = (s0 + k < n) ? po[(size_t)(s0 + k) * p.D + d] : 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc += (s0 + k < n) ? w[s0 + k] * v[k] : 0.f;
+        }
         merge_store(p.out, row * p.D + d, acc * inv, p.out_dtype);
     }
 }
