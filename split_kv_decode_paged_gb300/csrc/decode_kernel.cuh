@@ -43,6 +43,7 @@ constexpr int kOrderBuckets = 64;  // length buckets of the partial-chunk dispat
 constexpr int kFlagFirst = 1;
 constexpr int kFlagLast = 2;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kMaxSlack = 8.f;  // log2 headroom of the softmax reference maximum
 
 struct StageMeta {
     int b, kvh, s, t0, nvalid, flags, nsplit, vlo;  // b: KV row; valid tile rows [vlo, nvalid)
@@ -691,26 +692,47 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             float sc = scale_log2;
             if constexpr (FP8) sc *= mt.kscale[r0 / p.boxr];
             const bool v0 = g >= lo_loc && g < nloc, v1 = (g + 8) >= lo_loc && (g + 8) < nloc;
+            // Scaled, masked scores.  The reference maximum mrow only moves
+            // when some score exceeds it by more than kMaxSlack (log2 units):
+            // softmax does not depend on the reference, and the weights stay
+            // <= 2^kMaxSlack.  Then the warp reduces the tile's row maxima
+            // (three shuffle rounds) and rescales; otherwise it skips both.
+            float sv[NT][4];
+            bool need = false;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                sv[n][0] = v0 ? sacc[n][0] * sc : -INFINITY;
+                sv[n][1] = v0 ? sacc[n][1] * sc : -INFINITY;
+                sv[n][2] = v1 ? sacc[n][2] * sc : -INFINITY;
+                sv[n][3] = v1 ? sacc[n][3] * sc : -INFINITY;
+                need |= fmaxf(sv[n][0], sv[n][2]) > mrow[n][0] + kMaxSlack;
+                need |= fmaxf(sv[n][1], sv[n][3]) > mrow[n][1] + kMaxSlack;
+            }
             float alpha[NT][2];
+            const bool moved = __any_sync(0xffffffffu, need);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                alpha[n][0] = alpha[n][1] = 1.f;
+                if (moved) {
+                    float mx0 = fmaxf(sv[n][0], sv[n][2]), mx1 = fmaxf(sv[n][1], sv[n][3]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, shfl_xor(mx0, off));
+                        mx1 = fmaxf(mx1, shfl_xor(mx1, off));
+                    }
+                    const float mn0 = fmaxf(mrow[n][0], mx0), mn1 = fmaxf(mrow[n][1], mx1);
+                    alpha[n][0] = (mn0 == -INFINITY) ? 1.f : ex2(mrow[n][0] - mn0);
+                    alpha[n][1] = (mn1 == -INFINITY) ? 1.f : ex2(mrow[n][1] - mn1);
+                    mrow[n][0] = mn0;
+                    mrow[n][1] = mn1;
+                }
+            }
             uint32_t pb[NT][2];
             uint32_t pl[NT][2];  // bf16 V: low parts of the weights (P = hi + lo)
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const float s0 = v0 ? sacc[n][0] * sc : -INFINITY;
-                const float s1 = v0 ? sacc[n][1] * sc : -INFINITY;
-                const float s2 = v1 ? sacc[n][2] * sc : -INFINITY;
-                const float s3 = v1 ? sacc[n][3] * sc : -INFINITY;
-                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, shfl_xor(mx0, off));
-                    mx1 = fmaxf(mx1, shfl_xor(mx1, off));
-                }
-                const float mn0 = fmaxf(mrow[n][0], mx0), mn1 = fmaxf(mrow[n][1], mx1);
-                alpha[n][0] = (mn0 == -INFINITY) ? 1.f : ex2(mrow[n][0] - mn0);
-                alpha[n][1] = (mn1 == -INFINITY) ? 1.f : ex2(mrow[n][1] - mn1);
-                mrow[n][0] = mn0;
-                mrow[n][1] = mn1;
+                const float mn0 = mrow[n][0], mn1 = mrow[n][1];
+                const float s0 = sv[n][0], s1 = sv[n][1], s2 = sv[n][2], s3 = sv[n][3];
                 const float p0 = (mn0 == -INFINITY) ? 0.f : ex2(s0 - mn0);
                 const float p1 = (mn1 == -INFINITY) ? 0.f : ex2(s1 - mn1);
                 const float p2 = (mn0 == -INFINITY) ? 0.f : ex2(s2 - mn0);
@@ -743,19 +765,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 pb[n][0] = movmatrix_t(x0);
                 pb[n][1] = movmatrix_t(x1);
             }
+            if (moved) {
 #pragma unroll
-            for (int mi = 0; mi < MT; ++mi)
+                for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    o[mi][n][0] *= alpha[n][0];
-                    o[mi][n][1] *= alpha[n][1];
-                    o[mi][n][2] *= alpha[n][0];
-                    o[mi][n][3] *= alpha[n][1];
-                }
+                    for (int n = 0; n < NT; ++n) {
+                        o[mi][n][0] *= alpha[n][0];
+                        o[mi][n][1] *= alpha[n][1];
+                        o[mi][n][2] *= alpha[n][0];
+                        o[mi][n][3] *= alpha[n][1];
+                    }
+            }
 
             // ---------------------------------------------------- O^T += V^T P^T
+            // Rows outside [lo_loc, nloc) may hold any bits (stale or NaN):
+            // partial sub-tiles zero their V fragments.
+            const bool part = nloc < kTokensPerWarp || lo_loc > 0;
             uint32_t msk01 = 0xffffffffu, msk23 = 0xffffffffu;
-            if (nloc < kTokensPerWarp || lo_loc > 0) {
+            if (part) {
                 auto ok_t = [&](int t) { return t >= lo_loc && t < nloc; };
                 msk01 = (ok_t(2 * c) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 1) ? 0xffff0000u : 0u);
                 msk23 = (ok_t(2 * c + 8) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 9) ? 0xffff0000u : 0u);
@@ -768,7 +795,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const int chunk = (byte % SUBROW) / 16 + ((lane >> 3) & 1);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_t, chunk), a0, a1, a2, a3);
-                    a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23;
+                    if (part) { a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23; }
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         if constexpr (KV == KV_BF16) {
@@ -788,17 +815,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
                     uint32_t q0, q1, q2, q3;
                     ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
+                    // the 16-bit halves of q0, q2 hold tokens 2c, 2c+1; of q1,
+                    // q3 tokens 2c+8, 2c+9 (E4M3 zero bytes convert to +0)
+                    if (part) { q0 &= msk01; q1 &= msk23; q2 &= msk01; q3 &= msk23; }
                     const uint32_t t0 = __byte_perm(q0, 0, 0x3120), t1 = __byte_perm(q1, 0, 0x3120);
                     const uint32_t t2 = __byte_perm(q2, 0, 0x3120), t3 = __byte_perm(q3, 0, 0x3120);
                     uint32_t A[2][4];
-                    A[0][0] = e4m3x2_to_f16x2((uint16_t)(t0 & 0xffff)) & msk01;
-                    A[0][1] = e4m3x2_to_f16x2((uint16_t)(t0 >> 16)) & msk01;
-                    A[0][2] = e4m3x2_to_f16x2((uint16_t)(t1 & 0xffff)) & msk23;
-                    A[0][3] = e4m3x2_to_f16x2((uint16_t)(t1 >> 16)) & msk23;
-                    A[1][0] = e4m3x2_to_f16x2((uint16_t)(t2 & 0xffff)) & msk01;
-                    A[1][1] = e4m3x2_to_f16x2((uint16_t)(t2 >> 16)) & msk01;
-                    A[1][2] = e4m3x2_to_f16x2((uint16_t)(t3 & 0xffff)) & msk23;
-                    A[1][3] = e4m3x2_to_f16x2((uint16_t)(t3 >> 16)) & msk23;
+                    A[0][0] = e4m3x2_to_f16x2((uint16_t)(t0 & 0xffff));
+                    A[0][1] = e4m3x2_to_f16x2((uint16_t)(t0 >> 16));
+                    A[0][2] = e4m3x2_to_f16x2((uint16_t)(t1 & 0xffff));
+                    A[0][3] = e4m3x2_to_f16x2((uint16_t)(t1 >> 16));
+                    A[1][0] = e4m3x2_to_f16x2((uint16_t)(t2 & 0xffff));
+                    A[1][1] = e4m3x2_to_f16x2((uint16_t)(t2 >> 16));
+                    A[1][2] = e4m3x2_to_f16x2((uint16_t)(t3 & 0xffff));
+                    A[1][3] = e4m3x2_to_f16x2((uint16_t)(t3 >> 16));
 #pragma unroll
                     for (int hs = 0; hs < 2; ++hs)
 #pragma unroll
