@@ -388,6 +388,107 @@ def bench_cascade(args):
         "gpu_launches_per_call": 3}))
 
 
+# ------------------------------------------------------- append and merge
+def _time_flushed(fn, steps, warmup, flush):
+    for _ in range(warmup):
+        l2_flush(flush)
+        fn()
+    ev = []
+    torch.cuda.nvtx.range_push("fd_timed")
+    for _ in range(steps):
+        l2_flush(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    ms = sorted(x.elapsed_time(y) for x, y in ev)
+    return statistics.median(ms) * 1e3, ms[len(ms) // 10] * 1e3, ms[(len(ms) * 9) // 10] * 1e3
+
+
+def bench_append(args):
+    """fd_append_kv (one new K and V row per sequence and KV head written into
+    the paged pools) on the GQA-batch pools (bf16) and the mixed FP8 pools
+    (bf16 rows quantised to E4M3 with the page's scale), L2 flushed before
+    every call."""
+    from split_kv_decode_paged_gb300 import workloads as W
+    import split_kv_decode_paged_gb300 as fd
+    from split_kv_decode_paged_gb300 import build as fd_build
+    fd_build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
+    peak, kind = measured_peak()
+    cases = {}
+    for c in (3, 5):
+        wl = W.make_config(c, dev)
+        spec = wl.spec
+        B, Hkv, D = spec.B, spec.Hkv, spec.D
+        in_dtype = wl.q.dtype if wl.k_pages.dtype == torch.float8_e4m3fn else wl.k_pages.dtype
+        g = torch.Generator(device=dev).manual_seed(77 + c)
+        k_new = torch.randn((B, Hkv, D), generator=g, device=dev).to(in_dtype)
+        v_new = torch.randn((B, Hkv, D), generator=g, device=dev).to(in_dtype)
+        pos = (wl.seq_lens - 1).clamp(min=0).to(torch.int32)  # rewrite each sequence's last token
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def run():
+            fd.append_kv(wl.q.dtype, k_new, v_new, wl.k_pages, wl.v_pages, wl.block_table, pos,
+                         wl.k_scale, wl.v_scale, status=status)
+
+        med, p10, p90 = _time_flushed(run, args.steps, args.warmup, flush)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"append flagged status {int(status.item())}")
+        e_in, e_c = k_new.element_size(), wl.k_pages.element_size()
+        nbytes = B * Hkv * D * 2 * (e_in + e_c) + 8 * B + (8 * B * Hkv if e_c == 1 else 0)
+        cases[f"config {c}"] = {"workload": f"{spec.name}: B={B}, Hkv={Hkv}, D={D}, {spec.kv} pages of {spec.page_size}",
+                                "us_median": med, "us_p10": p10, "us_p90": p90, "bytes": nbytes,
+                                "gbs": nbytes / med / 1e3}
+        del wl
+        torch.cuda.empty_cache()
+    head = cases["config 3"]
+    print(json.dumps({
+        "metric": "fd_append_kv achieved GB/s", "value": head["gbs"], "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "us_per_call": head["us_median"], "higher_is_better": True,
+        "dtype": "bf16 / e4m3", "data": "synthetic", "cases": cases, "peak": peak, "peak_source": kind,
+        "config": {"workload": "append one token per sequence into the GQA-batch and FP8-batch pools",
+                   "l2": "flushed before every timed call (write, then read, of 256 MB)"},
+        "gpu_launches_per_call": 1}))
+
+
+def bench_merge(args):
+    """fd_merge_states on fp32 partial states [B=64, Hq=32, S=8, D=128] to a
+    bf16 output, L2 flushed before every call."""
+    import split_kv_decode_paged_gb300 as fd
+    from split_kv_decode_paged_gb300 import build as fd_build
+    fd_build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
+    B, Hq, S, D = 64, 32, 8, 128
+    g = torch.Generator(device=dev).manual_seed(99)
+    o = torch.randn((B, Hq, S, D), generator=g, device=dev)
+    m = torch.randn((B, Hq, S), generator=g, device=dev) * 4
+    d = torch.rand((B, Hq, S), generator=g, device=dev) * 10 + 0.5
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    from split_kv_decode_paged_gb300 import _lib
+
+    def run():
+        _lib.fd_merge_states(o, m, d, out, lse, None)
+
+    med, p10, p90 = _time_flushed(run, args.steps, args.warmup, flush)
+    nbytes = B * Hq * S * (D + 2) * 4 + B * Hq * D * 2 + 4 * B * Hq
+    peak, kind = measured_peak()
+    print(json.dumps({
+        "metric": "fd_merge_states achieved GB/s", "value": nbytes / med / 1e3, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "us_per_call": med, "us_p10": p10, "us_p90": p90,
+        "higher_is_better": True, "dtype": "f32 partials -> bf16", "data": "synthetic", "bytes": nbytes,
+        "peak": peak, "peak_source": kind,
+        "config": {"workload": f"merge of partial states B={B}, Hq={Hq}, S={S}, D={D}",
+                   "l2": "flushed before every timed call (write, then read, of 256 MB)"},
+        "gpu_launches_per_call": 1}))
+
+
 # ------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -399,18 +500,20 @@ def main():
     ap.add_argument("--all-configs", action="store_true", help="also report every workload (per_config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", default="decode", choices=["decode", "cascade"],
-                    help="cascade: shared-prefix batch, cascade vs plain decode")
+    ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge"],
+                    help="cascade: shared-prefix batch, cascade vs plain decode; append: fd_append_kv; "
+                         "merge: fd_merge_states")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed decode calls (no warm-L2/graph/e2e extras, no CPU baseline)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
-    if args.workload == "cascade":
+    if args.workload != "decode":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the cascade workload is measured on the GPU path only"}))
+            print(json.dumps({"impl": "reference",
+                              "unavailable": f"the {args.workload} workload is measured on the GPU path only"}))
             return
-        bench_cascade(args)
+        {"cascade": bench_cascade, "append": bench_append, "merge": bench_merge}[args.workload](args)
         return
     from split_kv_decode_paged_gb300 import workloads as W
     ws, rank, local = dist_env()

@@ -74,6 +74,16 @@ __global__ void __launch_bounds__(kAppendWarps * 32) fd_append_kv_kernel(const A
     const int which = (int)(job & 1);
     const int bk = (int)(job >> 1);
     const int b = bk / p.Hkv, kvh = bk - (bk / p.Hkv) * p.Hkv;
+    const size_t src = ((size_t)b * p.Hkv + kvh) * p.D;
+    const void *in = which ? p.v_new : p.k_new;
+    // The new row does not depend on where it goes: request it before the
+    // seq_lens -> block table -> page chain (16-bit bits, D <= 256).
+    uint16_t raw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int d = lane + 32 * k;
+        raw[k] = d < p.D ? reinterpret_cast<const uint16_t *>(in)[src + d] : (uint16_t)0;
+    }
     const int L = p.seq_lens[b];
     const int col = L >= 0 ? L / p.page_size : -1;
     int page = -1;
@@ -87,16 +97,18 @@ __global__ void __launch_bounds__(kAppendWarps * 32) fd_append_kv_kernel(const A
         return;
     }
     const int slot = L - col * p.page_size;
-    const size_t src = ((size_t)b * p.Hkv + kvh) * p.D;
     const size_t dst = (((size_t)page * p.page_size + slot) * p.Hkv + kvh) * p.D;
-    const void *in = which ? p.v_new : p.k_new;
     void *pool = which ? p.v_pages : p.k_pages;
     const bool rot_k = rotary && which == 0;  // V is never rotated
     if (p.kv_kind != KV_E4M3) {
         const uint16_t *s16 = reinterpret_cast<const uint16_t *>(in) + src;
         uint16_t *d16 = reinterpret_cast<uint16_t *>(pool) + dst;
         if (!rot_k) {
-            for (int d = lane; d < p.D; d += 32) d16[d] = s16[d];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int d = lane + 32 * k;
+                if (d < p.D) d16[d] = raw[k];
+            }
             return;
         }
         const bool bf = p.kv_kind == KV_BF16;
@@ -108,9 +120,22 @@ __global__ void __launch_bounds__(kAppendWarps * 32) fd_append_kv_kernel(const A
     uint8_t *d8 = reinterpret_cast<uint8_t *>(pool) + dst;
     const void *srow = reinterpret_cast<const uint16_t *>(in) + src;
     auto x = [&](int d) { return load_16bit_as_float(srow, d, p.new_is_bf16); };
+    if (!rot_k) {
+        // element lane + 32k sits in raw[k]; one byte per element
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int d = lane + 32 * k;
+            if (d < p.D) {
+                const float xv = p.new_is_bf16 ? __uint_as_float(static_cast<uint32_t>(raw[k]) << 16)
+                                               : __half2float(__ushort_as_half(raw[k]));
+                d8[d] = (uint8_t)(f32x2_to_e4m3x2(0.f, __fdiv_rn(xv, sc)) & 0xffu);
+            }
+        }
+        return;
+    }
     for (int d = 2 * lane; d < p.D; d += 64) {
-        const float x0 = rot_k ? rotate_elem(p, x, d, L) : x(d);
-        const float x1 = rot_k ? rotate_elem(p, x, d + 1, L) : x(d + 1);
+        const float x0 = rotate_elem(p, x, d, L);
+        const float x1 = rotate_elem(p, x, d + 1, L);
         const uint16_t codes = f32x2_to_e4m3x2(__fdiv_rn(x1, sc), __fdiv_rn(x0, sc));
         *reinterpret_cast<uint16_t *>(d8 + d) = codes;
     }

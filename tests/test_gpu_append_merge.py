@@ -94,3 +94,41 @@ def test_merge_states_vs_oracle(fdlib, out_dtype):
                 assert gl == -np.inf and not got.any()
             else:
                 assert abs(gl - rl) < 1e-5
+
+
+def _merge_case(B, Hq, S, D, seed, offset=0):
+    g = torch.Generator().manual_seed(seed)
+    n = B * Hq * S * D
+    buf = torch.empty(n + offset, dtype=torch.float32)
+    o = buf[offset:].view(B, Hq, S, D)
+    o.copy_(torch.randn((B, Hq, S, D), generator=g))
+    m = torch.randn((B, Hq, S), generator=g) * 4
+    d = torch.rand((B, Hq, S), generator=g) * 10 + 0.5
+    m[0, 0, S // 2] = -float("inf"); d[0, 0, S // 2] = 0; o[0, 0, S // 2] = 0   # an empty chunk
+    m[B - 1, Hq - 1, :] = -float("inf"); d[B - 1, Hq - 1, :] = 0; o[B - 1, Hq - 1] = 0  # an all-empty row
+    return buf, o, m, d
+
+
+@pytest.mark.parametrize("S,D,offset", [(1, 128, 0), (9, 96, 0), (40, 64, 0), (33, 50, 0), (70, 33, 0),
+                                        (8, 256, 0), (12, 128, 1)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_merge_states_shapes_vs_oracle(fdlib, S, D, offset, out_dtype):
+    """Odd head sizes, more than 32 splits and a partial-state base that is only
+    4-byte aligned (scalar loads) against the oracle's merge."""
+    B, Hq = 2, 3
+    buf, o, m, d = _merge_case(B, Hq, S, D, 100 + S + D, offset)
+    gbuf = buf.cuda()
+    go = gbuf[offset:].view(B, Hq, S, D)
+    out, lse = fd.merge_states(go, m.cuda(), d.cuda(), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    tol = {torch.float32: 1e-5, torch.bfloat16: 2e-2}[out_dtype]
+    for b in range(B):
+        for h in range(Hq):
+            ro, rl = orc.merge_states(o[b, h].double().numpy(), m[b, h].double().numpy(), d[b, h].double().numpy())
+            got = out[b, h].double().cpu().numpy()
+            assert np.abs(got - ro).max() <= tol * max(1.0, np.abs(ro).max()), (b, h)
+            gl = float(lse[b, h])
+            if rl == -np.inf:
+                assert gl == -np.inf and not got.any()
+            else:
+                assert abs(gl - rl) < 1e-5
