@@ -255,28 +255,18 @@ def time_warm_and_graph(wl, dec, iters=50):
 
 
 def time_e2e(wl, dec, steps):
-    """End to end through the public API with host buffers: pinned H2D of the
-    step inputs (q, block table, seq_lens), the decode call, D2H of out and
-    lse, all inside the timed region.  The paged K/V cache is state that
-    lives in HBM across steps."""
-    q_h = wl.q.cpu().pin_memory()
-    bt_h = wl.block_table.cpu().pin_memory()
-    sl_h = wl.seq_lens.cpu().pin_memory()
-    q_d, bt_d, sl_d = torch.empty_like(wl.q), torch.empty_like(wl.block_table), torch.empty_like(wl.seq_lens)
-    out_d = torch.empty_like(wl.q)
-    lse_d = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=wl.q.device)
-    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
-    lse_h = torch.empty(lse_d.shape, dtype=torch.float32).pin_memory()
-    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    """End to end through the C ABI with host buffers (fd_decode_paged_host):
+    every step copies the packed pinned host block holding q, the block table
+    and seq_lens to the device (one copy), runs the decode, and copies the
+    packed out + lse block back (one copy), all inside the timed region.  The
+    paged K/V cache is state that lives in HBM across steps."""
+    io = dec.host_step()
+    io.q.copy_(wl.q.cpu())
+    io.block_table.copy_(wl.block_table.cpu())
+    io.seq_lens.copy_(wl.seq_lens.cpu())
 
     def step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        dec(q_d, wl.k_pages, wl.v_pages, bt_d, sl_d, k_scale=wl.k_scale, v_scale=wl.v_scale, out=out_d, lse=lse_d)
-        out_h.copy_(out_d, non_blocking=True)
-        lse_h.copy_(lse_d, non_blocking=True)
+        dec.step_host(io, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale)
 
     for _ in range(3):
         step()
@@ -287,7 +277,7 @@ def time_e2e(wl, dec, steps):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     dec.check()
-    return dt, h2d, d2h
+    return dt, io.layout.in_bytes, io.layout.out_bytes
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -621,7 +611,9 @@ def main():
         "graph_replay_us_per_call": None if args.quick else graph_ms * 1e3,
         "e2e": None if args.quick else {"value": bytes_call / e2e_s / 1e9, "unit": "GB/s",
                                         "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
-                                        "d2h_bytes_per_step": d2h},
+                                        "d2h_bytes_per_step": d2h,
+                                        "path": "fd_decode_paged_host: one pinned H2D copy of q + block table + "
+                                                "seq_lens, the decode, one D2H copy of out + lse per step"},
         "gpu_launches": args.steps * (1 if plan.fuse_merge or plan.num_splits == 1 else 2),
         "clocks": clk.summary(), "wall_s_timed_region": wall,
     }

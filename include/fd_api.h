@@ -296,6 +296,45 @@ fd_status fd_append_kv_rotary(const fd_problem *problem, const void *k_new, cons
                               const float *rotary_sin, int rotary_dim, int max_pos,
                               int interleaved, void *q_inout, int32_t *status_dev, void *stream);
 
+/* One decode step from and to host memory.  (The pages have no counterpart:
+ * a convenience of this library for serving loops whose per-step inputs are
+ * prepared on the host.)
+ *
+ * The step's inputs live in one host block and its results in another, so a
+ * step is one host-to-device copy, the decode (fd_decode_paged), and one
+ * device-to-host copy, all queued on `stream`:
+ *   input block   q [B, Hq, D] (q_dtype) at q_offset,
+ *                 block_table int32 [kv_rows, max_blocks_per_seq] at
+ *                 block_table_offset, seq_lens int32 [kv_rows] at
+ *                 seq_lens_offset; in_bytes in all
+ *   output block  out [B, Hq, D] (out_dtype) at out_offset, lse fp32 [B, Hq]
+ *                 at lse_offset; out_bytes in all
+ * Offsets are multiples of 256 bytes; kv_rows is the plan's (B unless the
+ * plan folds sequences onto shared KV rows). */
+typedef struct {
+    size_t q_offset, block_table_offset, seq_lens_offset, in_bytes;
+    size_t out_offset, lse_offset, out_bytes;
+} fd_host_io_layout;
+
+/* Fill *layout for plan.  Returns FD_ERR_INVALID_ARG on NULL arguments. */
+fd_status fd_host_io_layout_for(const fd_plan_t *plan, fd_host_io_layout *layout);
+
+/*   host_in    host input block (in_bytes), read by the copy; page-locked
+ *              (cudaHostAlloc / pinned) memory keeps the call asynchronous
+ *   dev_in     device buffer of in_bytes, 256-byte aligned, overwritten
+ *   dev_out    device buffer of out_bytes, 256-byte aligned, overwritten
+ *   host_out   host output block (out_bytes), written by the copy: valid once
+ *              `stream` has been synchronised
+ *   other arguments as fd_decode_paged (pools, scales, workspace, status_dev).
+ * Errors as fd_decode_paged; FD_ERR_CUDA when a copy cannot be queued.  The
+ * caller owns all four blocks and must not change host_in or read host_out
+ * until the stream has passed the call. */
+fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void *dev_in,
+                               const void *k_pages, const void *v_pages, const float *k_scale,
+                               const float *v_scale, void *dev_out, void *host_out,
+                               void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                               void *stream);
+
 /* Map a device status word to a status code (FD_OK when zero). */
 fd_status fd_status_from_device(int32_t status_word);
 

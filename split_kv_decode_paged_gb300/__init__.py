@@ -15,7 +15,7 @@ from . import _lib
 from ._lib import (FD_BF16, FD_E4M3, FD_F16, FD_F32, FdError, fd_append_kv, fd_decode_paged, fd_merge_states,
                    fd_plan, fd_status_from_device, fd_status_string, make_problem)
 
-__all__ = ["PagedDecoder", "fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string",
+__all__ = ["PagedDecoder", "HostStep", "fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string",
            "fd_status_from_device", "make_problem", "FdError", "append_kv", "merge_states"]
 
 
@@ -55,6 +55,18 @@ class PagedDecoder:
                         self.workspace, self.status, stream)
         return out, lse
 
+    def host_step(self):
+        """Pinned host and device blocks for step_host (see HostStep)."""
+        return HostStep(self)
+
+    def step_host(self, io, k_pages, v_pages, k_scale=None, v_scale=None, stream=None):
+        """One decode step from host memory: io.q, io.block_table and
+        io.seq_lens (pinned host views) are copied in with one copy, the
+        decode runs, and io.out and io.lse are copied back with one copy.
+        Asynchronous: synchronise the stream before reading io.out."""
+        _lib.fd_decode_paged_host(self.plan, io.host_in, io.dev_in, k_pages, v_pages, k_scale, v_scale, io.dev_out,
+                                  io.host_out, self.workspace, self.status, stream)
+
     def check(self):
         """Synchronise and raise FdError if the device reported an error."""
         word = int(self.status.item())
@@ -80,3 +92,31 @@ def merge_states(o_part, m, d, out_dtype=torch.float32, want_lse=True, stream=No
     lse = torch.empty((B, Hq), dtype=torch.float32, device=o_part.device) if want_lse else None
     fd_merge_states(o_part, m, d, out, lse, stream)
     return out, lse
+
+
+class HostStep:
+    """The host-side blocks of fd_decode_paged_host for one decoder: a pinned
+    input block holding q, block_table and seq_lens, a pinned output block
+    holding out and lse (typed views of both), and their device twins."""
+
+    def __init__(self, dec: PagedDecoder):
+        p, plan = dec.problem, dec.plan
+        lay = _lib.fd_host_io_layout_for(plan)
+        self.layout = lay
+        self.host_in = torch.empty(lay.in_bytes, dtype=torch.uint8).pin_memory()
+        self.host_out = torch.empty(lay.out_bytes, dtype=torch.uint8).pin_memory()
+        self.dev_in = torch.empty(lay.in_bytes, dtype=torch.uint8, device=dec.device)
+        self.dev_out = torch.empty(lay.out_bytes, dtype=torch.uint8, device=dec.device)
+        qt, ot = _lib.FD_TO_TORCH[p.q_dtype], _lib.FD_TO_TORCH[p.out_dtype]
+        kv_rows = plan.kv_rows if plan.kv_rows > 0 else p.B
+
+        def view(buf, off, n, dtype, shape):
+            nb = n * torch.empty((), dtype=dtype).element_size()
+            return buf[off:off + nb].view(dtype).view(shape)
+
+        self.q = view(self.host_in, lay.q_offset, p.B * p.Hq * p.D, qt, (p.B, p.Hq, p.D))
+        self.block_table = view(self.host_in, lay.block_table_offset, kv_rows * p.max_blocks_per_seq, torch.int32,
+                                (kv_rows, p.max_blocks_per_seq))
+        self.seq_lens = view(self.host_in, lay.seq_lens_offset, kv_rows, torch.int32, (kv_rows,))
+        self.out = view(self.host_out, lay.out_offset, p.B * p.Hq * p.D, ot, (p.B, p.Hq, p.D))
+        self.lse = view(self.host_out, lay.lse_offset, p.B * p.Hq, torch.float32, (p.B, p.Hq))

@@ -73,6 +73,12 @@ class FdPlan(ctypes.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_ if n not in ("problem", "reserved")}
 
 
+class FdHostIoLayout(ctypes.Structure):
+    _fields_ = [("q_offset", ctypes.c_size_t), ("block_table_offset", ctypes.c_size_t),
+                ("seq_lens_offset", ctypes.c_size_t), ("in_bytes", ctypes.c_size_t),
+                ("out_offset", ctypes.c_size_t), ("lse_offset", ctypes.c_size_t), ("out_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 
 
@@ -100,6 +106,10 @@ def load(path: str = LIB_PATH):
     L.fd_append_kv_rotary.argtypes = [ctypes.POINTER(FdProblem), P, P, P, P, P, P, P, P, P, P, I, I, I, P, P, P]
     L.fd_merge_two.restype = I
     L.fd_merge_two.argtypes = [P, P, P, P, I, I, I, P, P, P]
+    L.fd_host_io_layout_for.restype = I
+    L.fd_host_io_layout_for.argtypes = [ctypes.POINTER(FdPlan), ctypes.POINTER(FdHostIoLayout)]
+    L.fd_decode_paged_host.restype = I
+    L.fd_decode_paged_host.argtypes = [ctypes.POINTER(FdPlan), P, P, P, P, P, P, P, P, P, S, P, P]
     L.fd_status_string.restype = ctypes.c_char_p
     L.fd_status_string.argtypes = [I]
     L.fd_status_from_device.restype = I
@@ -219,3 +229,21 @@ def fd_merge_two(out_a, lse_a, out_b, lse_b, out, lse=None, stream=None):
                              _ptr(out), _ptr(lse), _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_merge_two")
+
+
+def fd_host_io_layout_for(plan: FdPlan) -> FdHostIoLayout:
+    lay = FdHostIoLayout()
+    rc = load().fd_host_io_layout_for(ctypes.byref(plan), ctypes.byref(lay))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_host_io_layout_for")
+    return lay
+
+
+def fd_decode_paged_host(plan: FdPlan, host_in, dev_in, k_pages, v_pages, k_scale, v_scale, dev_out, host_out,
+                         workspace, status=None, stream=None):
+    rc = load().fd_decode_paged_host(ctypes.byref(plan), _ptr(host_in), _ptr(dev_in), _ptr(k_pages), _ptr(v_pages),
+                                     _ptr(k_scale), _ptr(v_scale), _ptr(dev_out), _ptr(host_out), _ptr(workspace),
+                                     int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                     _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_decode_paged_host")

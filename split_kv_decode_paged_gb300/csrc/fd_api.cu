@@ -496,6 +496,46 @@ fd_status fd_decode_paged_ex(const fd_plan_t *plan, const void *q, const void *k
                        workspace, workspace_bytes, status_dev, stream);
 }
 
+fd_status fd_host_io_layout_for(const fd_plan_t *plan, fd_host_io_layout *layout) {
+    if (!plan || !layout) return FD_ERR_INVALID_ARG;
+    const fd_problem &p = plan->problem;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t rows = (size_t)p.B * p.Hq;
+    const size_t kv_rows = (size_t)(plan->kv_rows > 0 ? plan->kv_rows : p.B);
+    layout->q_offset = 0;
+    layout->block_table_offset = up(rows * p.D * elem_bytes(p.q_dtype));
+    layout->seq_lens_offset = layout->block_table_offset + up(kv_rows * p.max_blocks_per_seq * 4);
+    layout->in_bytes = layout->seq_lens_offset + up(kv_rows * 4);
+    layout->out_offset = 0;
+    layout->lse_offset = up(rows * p.D * elem_bytes(p.out_dtype));
+    layout->out_bytes = layout->lse_offset + up(rows * 4);
+    return FD_OK;
+}
+
+fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void *dev_in, const void *k_pages,
+                               const void *v_pages, const float *k_scale, const float *v_scale, void *dev_out,
+                               void *host_out, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                               void *stream) {
+    if (!plan || !host_in || !dev_in || !dev_out || !host_out) return FD_ERR_INVALID_ARG;
+    if (!aligned(dev_in, 256) || !aligned(dev_out, 256)) return FD_ERR_INVALID_ARG;
+    fd_host_io_layout io;
+    fd_host_io_layout_for(plan, &io);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dev_in, host_in, io.in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return FD_ERR_CUDA;
+    uint8_t *in = static_cast<uint8_t *>(dev_in);
+    uint8_t *out = static_cast<uint8_t *>(dev_out);
+    const fd_status r = fd_decode_paged(plan, in + io.q_offset, k_pages, v_pages, k_scale, v_scale,
+                                        reinterpret_cast<const int32_t *>(in + io.block_table_offset),
+                                        reinterpret_cast<const int32_t *>(in + io.seq_lens_offset),
+                                        out + io.out_offset, reinterpret_cast<float *>(out + io.lse_offset),
+                                        workspace, workspace_bytes, status_dev, stream);
+    if (r != FD_OK) return r;
+    if (cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return FD_OK;
+}
+
 fd_status fd_merge_states(const float *o_part, const float *m, const float *d, int B, int Hq, int S, int D,
                           fd_dtype out_dtype, void *out, float *lse, void *stream) {
     if (!o_part || !m || !d || !out) return FD_ERR_INVALID_ARG;
