@@ -128,22 +128,69 @@ __device__ __forceinline__ size_t q_row(const DecodeParams &p, int bkv, int kvh,
 
 // Fused merge of the nsplit partial states of the nrows q rows of one
 // (KV row, kvh, head sub-group), run by the consumer warps of the CTA that
-// completed the last split.  alpha: >= nrows*nsplit floats.
+// completed the last split: m_g = max m_i, w_i = exp(m_i - m_g),
+// O = sum w_i O_i / sum w_i d_i, lse = m_g + log(sum w_i d_i).
+// alpha: >= nrows*nsplit floats of shared memory.
 template <int NC>
 __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int nrows, int qrows, int nsplit,
                             float *alpha, int warp, int lane, int D) {
     const int S = p.S;
+    const int tid = warp * 32 + lane;
+    constexpr int kFew = 8;
+    if (nsplit <= kFew) {
+        // Few splits: every thread reads the m, d and O of its four outputs
+        // for all splits in one round of loads and merges them itself.
+        for (int idx = tid; idx < nrows * (D / 4); idx += NC * 32) {
+            const int h = idx / (D / 4), d = (idx - h * (D / 4)) * 4;
+            const size_t row = q_row(p, b, kvh, hg, h, qrows);
+            float m[kFew], dd[kFew];
+            float4 v[kFew];
+#pragma unroll
+            for (int k = 0; k < kFew; ++k) {
+                const bool in = k < nsplit;
+                m[k] = in ? ldcg(p.part_m + row * S + k) : -INFINITY;
+                dd[k] = in ? ldcg(p.part_d + row * S + k) : 0.f;
+                v[k] = in ? __ldcg(reinterpret_cast<const float4 *>(p.part_o + (row * S + k) * D + d))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kFew; ++k) mx = fmaxf(mx, m[k]);
+            float sum = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kFew; ++k) {
+                const float a = (m[k] == -INFINITY) ? 0.f : __expf(m[k] - mx);
+                sum = fmaf(a, dd[k], sum);
+                acc.x = fmaf(a, v[k].x, acc.x);
+                acc.y = fmaf(a, v[k].y, acc.y);
+                acc.z = fmaf(a, v[k].z, acc.z);
+                acc.w = fmaf(a, v[k].w, acc.w);
+            }
+            const bool empty = (mx == -INFINITY) || !(sum > 0.f);
+            const float inv = empty ? 0.f : 1.f / sum;
+            store_out4(p.out, row * D + d, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.out_dtype);
+            if (d == 0 && p.lse) p.lse[row] = empty ? -INFINITY : mx + logf(sum);
+        }
+        return;
+    }
+    // Many splits: a warp per q row finds the weights (m and d read in one
+    // round), then the outputs in float4 groups with 8 split loads in flight.
     for (int h = warp; h < nrows; h += NC) {
         const size_t row = q_row(p, b, kvh, hg, h, qrows);
         const float *pm = p.part_m + row * S;
         const float *pd = p.part_d + row * S;
         float mx = -INFINITY;
-        for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, ldcg(pm + s));
+        for (int s = lane; s < nsplit; s += 32) {
+            const float ms = ldcg(pm + s);
+            alpha[h * nsplit + s] = ms;
+            mx = fmaxf(mx, ms);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float sum = 0.f;
         for (int s = lane; s < nsplit; s += 32) {
-            const float ms = ldcg(pm + s);
+            const float ms = alpha[h * nsplit + s];
             const float a = (ms == -INFINITY) ? 0.f : __expf(ms - mx);
             alpha[h * nsplit + s] = a;
             sum += a * ldcg(pd + s);
@@ -156,9 +203,6 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int n
         if (lane == 0 && p.lse) p.lse[row] = empty ? -INFINITY : mx + logf(sum);
     }
     named_bar_sync(1, NC * 32);
-    // Outputs in float4 groups; the split loop issues 8 independent L2 loads
-    // per batch so the merge is not one load latency per split.
-    const int tid = warp * 32 + lane;
     for (int idx = tid; idx < nrows * (D / 4); idx += NC * 32) {
         const int h = idx / (D / 4), d = (idx - h * (D / 4)) * 4;
         const size_t row = q_row(p, b, kvh, hg, h, qrows);
