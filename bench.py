@@ -49,8 +49,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the kernel sources plus fd_api.cu, which encodes the TMA maps (box shape,
+# swizzle, L2 promotion) that shape the kernel's DRAM traffic
 DECODE_KERNEL_FILES = ("decode_kernel.cuh", "decode_dispatch.cuh", "decode_f16.cu", "decode_bf16.cu",
-                       "decode_e4m3.cu", "ptx.cuh", "fd_internal.h")
+                       "decode_e4m3.cu", "ptx.cuh", "fd_internal.h", "fd_api.cu")
 
 
 def kernel_source_hash():

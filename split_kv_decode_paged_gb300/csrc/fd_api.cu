@@ -231,8 +231,13 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, const fd_problem &p, in
     cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
     const CUtensorMapDataType dt = e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
     const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    // L2 promotion no wider than one row: a wider promotion also fetches the
+    // neighbouring KV head's row, which another CTA reads at another time.
+    const CUtensorMapL2promotion l2p = rb >= 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : rb >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                   : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
     CUresult r = fn(map, dt, 5, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    l2p, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
