@@ -250,10 +250,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     StageMeta *meta = reinterpret_cast<StageMeta *>(reinterpret_cast<uint8_t *>(scratch) + align_up(Sh::SCRATCH, 128));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(meta + NST);
     uint64_t *empty_bar = full_bar + NST;
-    int *prefix = reinterpret_cast<int *>(empty_bar + NST);
-    int *lens = prefix + p.B + 1;
-    int *order = lens + p.B;
-    int *hist = order + p.B;  // kOrderBuckets
+    // Dispatch tables (sized for p.B >= the KV rows): item prefix at 32-row
+    // block boundaries, attended length per row, partial-chunk row order.
+    const int nblk = (p.B + 31) / 32;
+    int *bpre = reinterpret_cast<int *>(empty_bar + NST);  // nblk + 1
+    int *lens = bpre + nblk + 1;                           // B
+    int *hist = lens + p.B;                                // kOrderBuckets
+    uint16_t *order = reinterpret_cast<uint16_t *>(hist + kOrderBuckets);  // B
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -297,6 +300,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         //     an empty row), rows sorted by that chunk's length, longest first
         //     (stable counting sort into kOrderBuckets buckets).
         // Largest items go first and the smallest fill the tail.
+        // Attended length of every row: tokens [leftpad, seq_len) of its cache
+        // row.  No warp collective in this loop, so its loads overlap.
+        for (int b = lane; b < B; b += 32) {
+            const int cb = cache_row(b);
+            int L = 0;
+            if (cb >= 0) {
+                L = p.seq_lens[cb];
+                if (p.leftpad) {
+                    const int lp = p.leftpad[cb];
+                    L = (lp < 0 || lp > L) ? -1 : L - lp;
+                }
+            }
+            if (L < 0 || L > p.cap) {
+                flag_status(p.status, FD_DEV_CAPACITY);
+                L = L < 0 ? 0 : p.cap;
+            }
+            lens[b] = L;
+        }
         for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
         __syncwarp();
         const long long c1 = (long long)C + 1;
@@ -310,21 +331,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             int bucket = kOrderBuckets;  // sentinel: past B or no partial chunk
             int vA = 0;
             if (b < B) {
-                // Attended length: tokens [leftpad, seq_len) of the q row's cache row.
-                const int cb = cache_row(b);
-                int L = 0;
-                if (cb >= 0) {
-                    L = p.seq_lens[cb];
-                    if (p.leftpad) {
-                        const int lp = p.leftpad[cb];
-                        L = (lp < 0 || lp > L) ? -1 : L - lp;
-                    }
-                }
-                if (L < 0 || L > p.cap) {
-                    flag_status(p.status, FD_DEV_CAPACITY);
-                    L = L < 0 ? 0 : p.cap;
-                }
-                lens[b] = L;
+                const int L = lens[b];
                 vA = (L / C) * HG;
                 const int r = tail_of(L);
                 if (r >= 0) bucket = bucket_of(r);
@@ -332,15 +339,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const unsigned peers = __match_any_sync(0xffffffffu, bucket);
             if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, vA, o);
-                if (lane >= o) vA += t;
-            }
-            if (b < B) prefix[b + 1] = runningA + vA;
-            runningA += __shfl_sync(0xffffffffu, vA, 31);
+            for (int o = 16; o > 0; o >>= 1) vA += __shfl_xor_sync(0xffffffffu, vA, o);
+            if (lane == 0) bpre[base >> 5] = runningA;
+            runningA += vA;
             __syncwarp();
         }
-        if (lane == 0) prefix[0] = 0;
+        if (lane == 0) bpre[(B + 31) >> 5] = runningA;
         int nB = 0;
         {   // exclusive scan of the bucket counts (2 buckets per lane)
             const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
@@ -364,7 +368,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const unsigned peers = __match_any_sync(0xffffffffu, bucket);
             if (bucket < kOrderBuckets) {
                 const unsigned below = peers & ((1u << lane) - 1u);
-                order[hist[bucket] + __popc(below)] = b;
+                order[hist[bucket] + __popc(below)] = (uint16_t)b;
             }
             __syncwarp();
             if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
@@ -383,15 +387,27 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             Item it;
             int r2;
             if (item < totalA) {
-                int lo = 0, hi = B - 1;
+                // The 32-row block by binary search over the block prefix,
+                // then the row by a warp scan of the block's item counts.
+                int lo = 0, hi = ((B + 31) >> 5) - 1;
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
-                    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+                    if (bpre[mid] <= item) lo = mid; else hi = mid - 1;
                 }
-                it.b = lo;
+                const int bl = lo * 32 + lane;
+                const int v = bl < B ? (lens[bl] / C) * HG : 0;
+                int incl = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                const int off = item - bpre[lo];
+                const int ln = __ffs(__ballot_sync(0xffffffffu, incl > off)) - 1;
+                it.b = lo * 32 + ln;
                 // within a KV row: split-major, then kvh, then head sub-group
                 // (the sub-groups of one (split, kvh) read the same K/V back to back)
-                const int rem = item - prefix[lo];
+                const int rem = off - __shfl_sync(0xffffffffu, incl - v, ln);
                 it.s = rem / HG;
                 r2 = rem - it.s * HG;
             } else {
@@ -1010,7 +1026,7 @@ size_t decode_smem_for(int stages, int B) {
     n += align_up(Sh::SCRATCH, 128);
     n += (size_t)stages * sizeof(StageMeta);
     n += (size_t)stages * 16;
-    n += (size_t)(3 * B + 1 + kOrderBuckets) * 4;
+    n += (size_t)((B + 31) / 32 + 1 + B + kOrderBuckets) * 4 + (size_t)align_up(2 * B, 4);  // dispatch tables
     return n;
 }
 

@@ -224,3 +224,18 @@ def test_plan_reused_while_lengths_grow(fdlib):
                          wl.num_pages)
         ref_o, ref_l = oracle_full(cpu)
         assert_close("bf16", out, lse, ref_o, ref_l, f"grow step {step}")
+
+
+@pytest.mark.parametrize("B,splits,kv", [(100, 2, "bf16"), (1000, 3, "bf16"), (8192, 2, "bf16"), (2100, 2, "e4m3")])
+def test_large_batches_many_row_blocks(fdlib, B, splits, kv):
+    """Batches spanning many 32-row blocks of the dispatch tables (and the
+    maximum batch): ragged lengths with empty rows, rows shorter than one chunk
+    and rows split in several, so full-chunk and partial-chunk items both occur;
+    every (row, head) checked against the oracle."""
+    rng = np.random.default_rng(B + splits)
+    lens = rng.integers(0, 400, B)
+    lens[rng.choice(B, B // 10, replace=False)] = 0
+    lens[rng.choice(B, B // 20, replace=False)] = 256  # exactly two full 128-token tiles
+    spec = _spec(f"B={B}", B, 8, 2, 64, 16, kv, "bf16", lens.tolist())
+    err, dec = _run_and_check(spec, 7 + B, num_splits=splits)
+    assert dec.plan.num_splits > 1  # the requested count rounds to whole 128-token tiles
