@@ -101,7 +101,9 @@ typedef struct {
                            estimated time is within this many percent of the
                            best; 18 reproduces the cookbook's "smallest split
                            count reaching 85% of the best efficiency" [P3 §6.3] */
-    int tile_tokens;    /* 0 = default (128); 64 or 128 tokens per pipeline stage */
+    int tile_tokens;    /* tokens per pipeline stage: 64, 128, or 256 (E4M3 pools
+                           with page_size % 32 == 0); 0 = default: 256 for E4M3
+                           when pages allow and 3 stages fit, else 128 */
     int shared_kv;      /* 1: every q sequence attends the same KV row (one
                            block-table row, seq_lens[0]; e.g. a shared prefix):
                            the B*G q rows of each KV head are packed 16 to a

@@ -66,8 +66,11 @@ struct DecodeShape {
     static constexpr int Q_REGION = align_up(QROWS * D * 2, 1024);
     static constexpr int STAGE = 2 * KV_REGION + Q_REGION;
     static constexpr int SS = D + 4;                   // scratch row stride (floats)
-    // Per-warp O rows; reused for the merge weights (QROWS x kMaxSplits).
-    static constexpr int SCR_O = (NC * QROWS * SS > QROWS * kMaxSplits) ? NC * QROWS * SS : QROWS * kMaxSplits;
+    // Epilogue slots of per-warp O rows: with 8 or more consumer warps, warp
+    // w + NC/2 first hands its state to warp w, so half as many slots.
+    // Reused for the merge weights (QROWS x kMaxSplits).
+    static constexpr int NSLOT = NC >= 8 ? NC / 2 : NC;
+    static constexpr int SCR_O = (NSLOT * QROWS * SS > QROWS * kMaxSplits) ? NSLOT * QROWS * SS : QROWS * kMaxSplits;
     static constexpr int SCRATCH = SCR_O * 4 + 2 * NC * QROWS * 4 + 2 * QROWS * 4 + 16;
     static constexpr int THREADS = (NC + 1) * 32;
     static_assert(D == 64 || D == 128, "D");
@@ -923,29 +926,72 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 v += shfl_xor(v, 16);
                 lrow[n][r] = v;
             }
-        float *so = scratch + warp * QROWS * SS;
+        constexpr int NSLOT = Sh::NSLOT;
+        // Warp state (o, m, l) into epilogue slot `slot`.
+        auto put_state = [&](int slot) {
+            float *so = scratch + slot * QROWS * SS;
 #pragma unroll
-        for (int mi = 0; mi < MT; ++mi) {
-            const int d0 = FP8 ? 16 * mi + 2 * g : 16 * mi + g;
-            const int d1 = FP8 ? d0 + 1 : d0 + 8;
+            for (int mi = 0; mi < MT; ++mi) {
+                const int d0 = FP8 ? 16 * mi + 2 * g : 16 * mi + g;
+                const int d1 = FP8 ? d0 + 1 : d0 + 8;
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int h0 = n * 8 + 2 * c, h1 = h0 + 1;
-                so[h0 * SS + d0] = o[mi][n][0];
-                so[h1 * SS + d0] = o[mi][n][1];
-                so[h0 * SS + d1] = o[mi][n][2];
-                so[h1 * SS + d1] = o[mi][n][3];
+                for (int n = 0; n < NT; ++n) {
+                    const int h0 = n * 8 + 2 * c, h1 = h0 + 1;
+                    so[h0 * SS + d0] = o[mi][n][0];
+                    so[h1 * SS + d0] = o[mi][n][1];
+                    so[h0 * SS + d1] = o[mi][n][2];
+                    so[h1 * SS + d1] = o[mi][n][3];
+                }
             }
-        }
-        if (g == 0) {
+            if (g == 0) {
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int h0 = n * 8 + 2 * c;
-                scr_m[warp * QROWS + h0] = mrow[n][0];
-                scr_m[warp * QROWS + h0 + 1] = mrow[n][1];
-                scr_l[warp * QROWS + h0] = lrow[n][0];
-                scr_l[warp * QROWS + h0 + 1] = lrow[n][1];
+                for (int n = 0; n < NT; ++n) {
+                    const int h0 = n * 8 + 2 * c;
+                    scr_m[slot * QROWS + h0] = mrow[n][0];
+                    scr_m[slot * QROWS + h0 + 1] = mrow[n][1];
+                    scr_l[slot * QROWS + h0] = lrow[n][0];
+                    scr_l[slot * QROWS + h0 + 1] = lrow[n][1];
+                }
             }
+        };
+        if constexpr (NSLOT < NC) {
+            // Warp w + NSLOT hands its state to warp w, which merges it into
+            // its own registers (same rescale as the final combine).
+            if (warp >= NSLOT) put_state(warp - NSLOT);
+            named_bar_sync(1, NC * 32);
+            if (warp < NSLOT) {
+                const float *so = scratch + warp * QROWS * SS;
+                float wo[NT][2], wp[NT][2];
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int h = n * 8 + 2 * c + r;
+                        const float pm = scr_m[warp * QROWS + h], pl = scr_l[warp * QROWS + h];
+                        const float mn = fmaxf(mrow[n][r], pm);
+                        wo[n][r] = (mn == -INFINITY) ? 0.f : ex2(mrow[n][r] - mn);
+                        wp[n][r] = (mn == -INFINITY) ? 0.f : ex2(pm - mn);
+                        lrow[n][r] = wo[n][r] * lrow[n][r] + wp[n][r] * pl;
+                        mrow[n][r] = mn;
+                    }
+#pragma unroll
+                for (int mi = 0; mi < MT; ++mi) {
+                    const int d0 = FP8 ? 16 * mi + 2 * g : 16 * mi + g;
+                    const int d1 = FP8 ? d0 + 1 : d0 + 8;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const int h0 = n * 8 + 2 * c, h1 = h0 + 1;
+                        o[mi][n][0] = wo[n][0] * o[mi][n][0] + wp[n][0] * so[h0 * SS + d0];
+                        o[mi][n][1] = wo[n][1] * o[mi][n][1] + wp[n][1] * so[h1 * SS + d0];
+                        o[mi][n][2] = wo[n][0] * o[mi][n][2] + wp[n][0] * so[h0 * SS + d1];
+                        o[mi][n][3] = wo[n][1] * o[mi][n][3] + wp[n][1] * so[h1 * SS + d1];
+                    }
+                }
+                __syncwarp();  // every lane has read the slot before it is rewritten
+                put_state(warp);
+            }
+        } else {
+            put_state(warp);
         }
         named_bar_sync(1, NC * 32);
         const int tid = warp * 32 + lane;
@@ -956,10 +1002,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const int h = tid;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NC; ++w) M = fmaxf(M, scr_m[w * QROWS + h]);
+            for (int w = 0; w < NSLOT; ++w) M = fmaxf(M, scr_m[w * QROWS + h]);
             float Ls = 0.f;
 #pragma unroll
-            for (int w = 0; w < NC; ++w) {
+            for (int w = 0; w < NSLOT; ++w) {
                 const float a = (M == -INFINITY) ? 0.f : ex2(scr_m[w * QROWS + h] - M);
                 scr_m[w * QROWS + h] = a;
                 Ls += a * scr_l[w * QROWS + h];
@@ -980,7 +1026,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const int h = idx / (D / 4), d = (idx - h * (D / 4)) * 4;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < NC; ++w) {
+            for (int w = 0; w < NSLOT; ++w) {
                 const float a = scr_m[w * QROWS + h];
                 const float4 v = *reinterpret_cast<const float4 *>(scratch + (w * QROWS + h) * SS + d);
                 acc.x = fmaf(a, v.x, acc.x);

@@ -25,16 +25,19 @@ size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
 
 KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold) {
     KernelShape ks;
-    const int tile = tile_tokens == 64 ? 64 : 128;
+    // 256-token stages: E4M3 only, with pages of >= 32 tokens (at most
+    // kMaxBoxesPerTile boxes per stage).
+    const bool t256 = tile_tokens == 256 && p.kv_dtype == FD_E4M3 &&
+                      std::gcd(p.page_size, 256) * kMaxBoxesPerTile >= 256;
+    const int tile = tile_tokens == 64 ? 64 : (t256 ? 256 : 128);
     if (tile == 64) {
         ks.consumer_warps = 4;
         ks.subtiles = 1;
-    } else if (p.kv_dtype == FD_E4M3) {
-        ks.consumer_warps = 8;  // E4M3 needs more consumer issue per byte
-        ks.subtiles = 1;
     } else {
-        ks.consumer_warps = 4;
-        ks.subtiles = 2;
+        // 8 consumer warps, 16 tokens each per 128 (one sub-tile; E4M3 with
+        // 256-token stages: two).
+        ks.consumer_warps = 8;
+        ks.subtiles = tile / 128;
     }
     ks.tile = ks.consumer_warps * ks.subtiles * kTokensPerWarp;
     ks.nt = (p.Hq / p.Hkv) * fold <= 8 ? 1 : 2;
@@ -277,7 +280,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (options) opt = *options;
     if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 ||
         opt.split_margin_pct < 0 || opt.split_margin_pct > 100 ||
-        (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128))
+        (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128 && opt.tile_tokens != 256))
         return FD_ERR_INVALID_ARG;
     // shared_kv: every q sequence attends KV row 0 (one block-table row, one
     // seq_lens entry): the B*G q rows of a KV head are sliced into items.
@@ -306,7 +309,15 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         if (st != FD_OK) return st;
         sms = di.sms;
     }
-    const KernelShape ks = kernel_shape(p, opt.tile_tokens, fold);
+    // E4M3 pools default to 256-token stages (8 consumer warps x 2 sub-tiles)
+    // when the pages allow them and three stages fit; otherwise 128.
+    int tile_opt = opt.tile_tokens;
+    if (tile_opt == 0 && p.kv_dtype == FD_E4M3) {
+        const KernelShape k256 = kernel_shape(p, 256, fold);
+        if (k256.tile == 256 && (long long)decode_smem_bytes(p, k256, 3) <= smem_optin / std::max(1, opt.ctas_per_sm))
+            tile_opt = 256;
+    }
+    const KernelShape ks = kernel_shape(p, tile_opt, fold);
     const int tile = ks.tile;
     const int qrows = 8 * ks.nt;
     const int nhg = ((p.Hq / p.Hkv) * fold + qrows - 1) / qrows;

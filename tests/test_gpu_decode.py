@@ -239,3 +239,14 @@ def test_large_batches_many_row_blocks(fdlib, B, splits, kv):
     spec = _spec(f"B={B}", B, 8, 2, 64, 16, kv, "bf16", lens.tolist())
     err, dec = _run_and_check(spec, 7 + B, num_splits=splits)
     assert dec.plan.num_splits > 1  # the requested count rounds to whole 128-token tiles
+
+
+@pytest.mark.parametrize("ps,splits,Hq", [(128, 0, 16), (32, 3, 16), (64, 2, 32)])
+def test_fp8_256_token_stages(fdlib, ps, splits, Hq):
+    """E4M3 pools with 256-token stages (8 consumer warps x 2 sub-tiles, the
+    pairwise epilogue combine): ragged lengths, empty and one-token rows, rows
+    ending inside a stage, split and unsplit; G = 8 and G = 16 (two head tiles)."""
+    lens = [0, 1, 255, 256, 257, 700, 3000, 130]
+    spec = _spec(f"fp8 t256 ps={ps}", len(lens), Hq, 2, 128, ps, "e4m3", "bf16", lens)
+    err, dec = _run_and_check(spec, 11 + ps, num_splits=splits, tile_tokens=256)
+    assert dec.plan.tile_tokens == 256
