@@ -96,3 +96,23 @@ def test_head_subgroups_and_shared_kv(fdlib):
     plan = _lib.fd_plan(prob, [4096], num_sms=148, shared_kv=1, num_splits=1)
     assert plan.row_fold == 64 and plan.kv_rows == 1 and plan.head_subgroups == 16
     assert plan.work_items_hint == 8 * 16
+
+
+@pytest.mark.parametrize("kv,ps,B,tile_opt,want_tile,want_stages", [
+    (torch.float8_e4m3fn, 128, 256, 0, 256, 3),    # E4M3 default: 256-token stages when they fit
+    (torch.float8_e4m3fn, 32, 64, 0, 256, 3),
+    (torch.float8_e4m3fn, 16, 256, 0, 128, None),  # 16-token pages: 16 boxes per 256 tokens is too many
+    (torch.float8_e4m3fn, 128, 4096, 0, 128, None),  # dispatch tables leave no room for 3 x 256 tokens
+    (torch.float8_e4m3fn, 128, 256, 128, 128, None),  # explicit request
+    (torch.bfloat16, 128, 256, 256, 128, 3),       # 256-token stages are E4M3 only
+    (torch.bfloat16, 16, 1024, 0, 128, 3),
+    (torch.bfloat16, 16, 8192, 0, 128, 2),         # the largest batch still plans
+])
+def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
+    prob = _lib.make_problem(B, 64, 8, 128, ps, 4096 // ps, B * (4096 // ps), torch.bfloat16, kv)
+    plan = _lib.fd_plan(prob, [1000] * B, num_sms=152, tile_tokens=tile_opt)
+    assert plan.tile_tokens == want_tile
+    assert plan.chunk_tokens % plan.tile_tokens == 0
+    assert plan.smem_bytes <= 232448
+    if want_stages is not None:
+        assert plan.stages == want_stages
