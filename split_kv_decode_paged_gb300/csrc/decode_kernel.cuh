@@ -297,6 +297,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
             return cb;
         };
+        // Warm L2 with the block table (each CTA one slice of it) while the
+        // dispatch tables are built, so the first items' page ids hit L2.
+        {
+            const long long bt_bytes = (long long)p.cache_rows * p.max_blocks * (long long)sizeof(int32_t);
+            if (bt_bytes <= (4 << 20)) {
+                const char *bt = reinterpret_cast<const char *>(p.block_table);
+                for (int off = ((int)blockIdx.x * 32 + lane) * 128; off < (int)bt_bytes; off += (int)gridDim.x * 32 * 128)
+                    prefetch_l2(bt + off);
+            }
+        }
         // Dispatch order, identical in every CTA (it depends only on seq_lens):
         //  A: every full chunk (C tokens) of every KV row, in row order;
         //  B: the last, partial chunk of each row (or the single empty item of
@@ -453,18 +463,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         };
         // Item ids: CTA i starts with item i; later items come from the
         // atomic counter, offset by the grid size.
-        auto claim = [&]() -> int {
-            int item = 0;
-            if (lane == 0) item = (int)gridDim.x + atomicAdd(p.work_ctr, 1);
-            return __shfl_sync(0xffffffffu, item, 0);
-        };
-
         int st = 0;
         uint32_t ph = 0;
         bool ok = true;
         long long n_issued = 0;
         // One item of lookahead: the next item is claimed, and its first two
-        // batches of page ids requested, while the current one streams.
+        // batches of page ids requested, while the current one streams.  The
+        // claim's atomic is issued as an item starts and its result read once
+        // the item's first tile is on its way.
         int next_item = (int)blockIdx.x;
         Item nx{};
         int npg0 = -1, npg1 = -1;
@@ -476,12 +482,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         while (ok && next_item < total) {
             const Item cur = nx;
             int pg_cur = npg0, pg_nxt = npg1;
-            next_item = claim();
-            if (next_item < total) {
-                nx = decode_item(next_item);
-                npg0 = page_of(nx, lane);
-                npg1 = page_of(nx, 32 + lane);
-            }
+            int claim_raw = 0;
+            if (lane == 0) claim_raw = atomicAdd(p.work_ctr, 1);
             const int b = cur.b, s = cur.s, kvh = cur.kvh, nsplit = cur.nsplit;
             const int t_begin = cur.t_begin, t_end = cur.t_end, ntok = cur.ntok, ntiles = cur.ntiles;
             const int nbox = cur.nbox, box0 = cur.box0;
@@ -573,6 +575,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 }
                 ++n_issued;
                 if (++st == NST) { st = 0; ph ^= 1u; }
+                if (j == 0) {
+                    next_item = (int)gridDim.x + __shfl_sync(0xffffffffu, claim_raw, 0);
+                    if (next_item < total) {
+                        nx = decode_item(next_item);
+                        npg0 = page_of(nx, lane);
+                        npg1 = page_of(nx, 32 + lane);
+                    }
+                }
             }
         }
         // No more items to claim: the next grid in the stream may start
