@@ -250,3 +250,14 @@ def test_fp8_256_token_stages(fdlib, ps, splits, Hq):
     spec = _spec(f"fp8 t256 ps={ps}", len(lens), Hq, 2, 128, ps, "e4m3", "bf16", lens)
     err, dec = _run_and_check(spec, 11 + ps, num_splits=splits, tile_tokens=256)
     assert dec.plan.tile_tokens == 256
+
+
+@pytest.mark.parametrize("fuse", [1, 0])
+@pytest.mark.parametrize("L,splits,want", [(65536, 512, 512), (40000, 300, 157)])
+def test_many_splits_up_to_the_maximum(fdlib, L, splits, want, fuse):
+    """The largest split count (512 chunks of one 128-token tile) and a count
+    past 32 that is not a power of two: the merge's weights span several
+    lanes' worth of splits, fused (last-CTA) and in the separate kernel."""
+    spec = _spec(f"L={L} S={splits}", 2, 8, 2, 64, 64, "bf16", "bf16", [L, L // 3])
+    err, dec = _run_and_check(spec, 5 + splits, num_splits=splits, fuse_merge=fuse)
+    assert dec.plan.num_splits == want
