@@ -303,8 +303,9 @@ fd_status fd_append_kv_rotary(const fd_problem *problem, const void *k_new, cons
  * prepared on the host.)
  *
  * The step's inputs live in one host block and its results in another, so a
- * step is one host-to-device copy, the decode (fd_decode_paged), and one
- * device-to-host copy, all queued on `stream`:
+ * step is one host-to-device copy and the decode (fd_decode_paged), plus one
+ * device-to-host copy unless the output block is mapped (below), all queued
+ * on `stream`:
  *   input block   q [B, Hq, D] (q_dtype) at q_offset,
  *                 block_table int32 [kv_rows, max_blocks_per_seq] at
  *                 block_table_offset, seq_lens int32 [kv_rows] at
@@ -325,8 +326,11 @@ fd_status fd_host_io_layout_for(const fd_plan_t *plan, fd_host_io_layout *layout
  *              (cudaHostAlloc / pinned) memory keeps the call asynchronous
  *   dev_in     device buffer of in_bytes, 256-byte aligned, overwritten
  *   dev_out    device buffer of out_bytes, 256-byte aligned, overwritten
- *   host_out   host output block (out_bytes), written by the copy: valid once
- *              `stream` has been synchronised
+ *   host_out   host output block (out_bytes), valid once `stream` has been
+ *              synchronised.  Page-locked memory mapped for the device (any
+ *              cudaHostAlloc / pinned block under unified addressing) is
+ *              written by the decode kernel itself and no copy is queued;
+ *              other host memory is filled by a copy from dev_out
  *   other arguments as fd_decode_paged (pools, scales, workspace, status_dev).
  * Errors as fd_decode_paged; FD_ERR_CUDA when a copy cannot be queued.  The
  * caller owns all four blocks and must not change host_in or read host_out

@@ -540,14 +540,26 @@ fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void 
     if (cudaMemcpyAsync(dev_in, host_in, io.in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return FD_ERR_CUDA;
     uint8_t *in = static_cast<uint8_t *>(dev_in);
+    // When the host output block is page-locked memory mapped for the device
+    // (unified addressing), the kernel stores out and lse straight into it:
+    // no device-to-host copy follows the decode.
     uint8_t *out = static_cast<uint8_t *>(dev_out);
+    bool direct = false;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host_out) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+        attr.devicePointer != nullptr && aligned(attr.devicePointer, 256)) {
+        out = static_cast<uint8_t *>(attr.devicePointer);
+        direct = true;
+    } else {
+        cudaGetLastError();  // a pageable pointer is not an error here
+    }
     const fd_status r = fd_decode_paged(plan, in + io.q_offset, k_pages, v_pages, k_scale, v_scale,
                                         reinterpret_cast<const int32_t *>(in + io.block_table_offset),
                                         reinterpret_cast<const int32_t *>(in + io.seq_lens_offset),
                                         out + io.out_offset, reinterpret_cast<float *>(out + io.lse_offset),
                                         workspace, workspace_bytes, status_dev, stream);
     if (r != FD_OK) return r;
-    if (cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!direct && cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return FD_ERR_CUDA;
     return FD_OK;
 }

@@ -46,3 +46,29 @@ def test_host_step_matches_device_call_and_oracle(fdlib, spec):
     ro, rl = orc.decode_paged(p, wl.q, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale, wl.block_table,
                               wl.seq_lens)
     assert_close(spec.kv, io.out, io.lse, ro, rl, f"host step {spec.name}")
+
+
+def test_host_step_pageable_output_block_is_copied(fdlib):
+    """An output block in ordinary (pageable) host memory cannot be written by
+    the kernel: the call falls back to the device block plus a copy."""
+    from split_kv_decode_paged_gb300 import _lib
+    spec = CASES[0]
+    wl = W.make(spec, 32, "cpu")
+    g = wl.to("cuda")
+    dec = fd.PagedDecoder.for_pools(g.q, g.k_pages, g.v_pages, g.block_table, wl.seq_lens)
+    ref_out, ref_lse = dec(g.q, g.k_pages, g.v_pages, g.block_table, g.seq_lens, g.k_scale, g.v_scale)
+    io = dec.host_step()
+    io.q.copy_(wl.q)
+    io.block_table.copy_(wl.block_table)
+    io.seq_lens.copy_(wl.seq_lens)
+    pageable = torch.full((io.layout.out_bytes,), 0xFF, dtype=torch.uint8)  # not pinned
+    assert not pageable.is_pinned()
+    _lib.fd_decode_paged_host(dec.plan, io.host_in, io.dev_in, g.k_pages, g.v_pages, g.k_scale, g.v_scale,
+                              io.dev_out, pageable, dec.workspace, dec.status)
+    torch.cuda.synchronize()
+    dec.check()
+    lay = io.layout
+    n_out = ref_out.numel() * ref_out.element_size()
+    assert torch.equal(pageable[lay.out_offset:lay.out_offset + n_out], ref_out.cpu().view(torch.uint8).flatten())
+    n_lse = ref_lse.numel() * 4
+    assert torch.equal(pageable[lay.lse_offset:lay.lse_offset + n_lse], ref_lse.cpu().view(torch.uint8).flatten())
