@@ -56,13 +56,15 @@ DECODE_KERNEL_FILES = ("decode_kernel.cuh", "decode_dispatch.cuh", "decode_f16.c
 
 
 def kernel_source_hash():
-    """Hash of the sources that define the decode kernel (ties a committed
-    ncu traffic figure to the kernel it was measured on)."""
+    """Hash of the code that defines the decode kernel, comments and blank
+    lines left out (ties a committed ncu traffic figure to the kernel it was
+    measured on)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_decode_paged_gb300", "csrc")
     for f in DECODE_KERNEL_FILES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            code = [ln.split("//", 1)[0].rstrip() for ln in fh]
+        h.update(f.encode() + "\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,28 +5,32 @@
 // query head hq, softmax(q k^T / sqrt(D)) V over the tokens [0, seq_lens[b])
 // of its KV head kvh = hq / G, plus the log-sum-exp.
 //
-// Work decomposition.  A work item is (sequence b, split s, KV head kvh): the
-// contiguous token range [s*C, min(L_b, (s+1)*C)) of one KV head, with all G
-// query heads of the group packed into the same CTA so each K/V byte is read
-// once (lpnh.cn "进阶突破", KV-reused layout for GQA).  Sequences shorter than
-// one chunk are not split.  Items are numbered b-major (then s, then kvh) and
-// handed out by an atomic counter to a persistent grid.
+// Work decomposition.  A work item is (sequence b, split s, KV head kvh,
+// head sub-group): the contiguous token range [s*C, min(L_b, (s+1)*C)) of one
+// KV head, with the query heads of the group (up to 16 rows) packed into the
+// same CTA so each K/V byte is read once (lpnh.cn "进阶突破", KV-reused layout
+// for GQA).  Sequences shorter than one chunk are not split.  Items are
+// dispatched longest first -- every full chunk, then each sequence's partial
+// chunk sorted by length -- through an atomic counter to a persistent grid.
 //
 // CTA layout: NC consumer warps + 1 producer warp.
-//   producer: claims items, reads the block table a batch of 32 boxes ahead,
-//     and issues TMA tensor loads of K and V boxes (page-size x D slices of
-//     one KV head) into a ring of shared-memory stages, plus one bulk copy of
-//     the item's G query rows; stage hand-off through full/empty mbarriers.
-//   consumers: each warp takes 16 tokens of every stage:
+//   producer: claims items one ahead, reads the block table a batch of 32
+//     boxes ahead, and issues TMA tensor loads of K and V boxes (page-size x D
+//     slices of one KV head) into a ring of shared-memory stages, plus one
+//     bulk copy of the item's query rows; stage hand-off through full/empty
+//     mbarriers with bounded waits.
+//   consumers: each warp takes SUBT sub-tiles of 16 tokens of every stage:
 //     S^T[16 tok x 8 heads] = K[16 x D] . Q^T  (mma.sync m16n8k16, K from
 //     swizzled shared memory via ldmatrix, Q in registers),
-//     online softmax in the exp2 domain, P^T moved into the B operand with
-//     movmatrix, O^T[D x 8] += V^T[D x 16] . P^T (ldmatrix.trans on V).
-//     At the end of an item the warps merge their states through shared
-//     memory; a single-split item writes out/lse, a multi-split item writes
-//     its partial state (unnormalised O, m, d) and the CTA that completes
-//     the last split of a (b, kvh) merges all of them (atomic counter, no
-//     spin-wait), per the merge formula of stage two.
+//     online softmax in the exp2 domain (the reference maximum moves only when
+//     a score passes it by more than kMaxSlack), P^T moved into the B operand
+//     with movmatrix, O^T[D x 8] += V^T[D x 16] . P^T (ldmatrix.trans on V).
+//     At the end of an item the warps merge their states (warp w+NC/2 into
+//     warp w, then through shared memory); a single-split item writes
+//     out/lse, a multi-split item writes its partial state (unnormalised O,
+//     m, d) and the CTA that completes the last split of a group merges all
+//     of them (atomic counter, no spin-wait), per the merge formula of stage
+//     two.
 // FP8 (E4M3) K/V are converted to f16 in registers (exact); the per-(page,
 // KV head) scales multiply the scores and the P.V product.
 #pragma once
