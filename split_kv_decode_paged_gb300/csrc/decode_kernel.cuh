@@ -117,15 +117,6 @@ __device__ __forceinline__ void store_out4(void *out, size_t idx, float a, float
     }
 }
 
-__device__ __forceinline__ void store_out(void *out, size_t idx, float v, int out_dtype) {
-    if (out_dtype == FD_BF16)
-        reinterpret_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
-    else if (out_dtype == FD_F16)
-        reinterpret_cast<__half *>(out)[idx] = __float2half_rn(v);
-    else
-        reinterpret_cast<float *>(out)[idx] = v;
-}
-
 // Global q row (b * Hq + hq) of row j of head sub-group hg of (KV row bkv, kvh).
 __device__ __forceinline__ size_t q_row(const DecodeParams &p, int bkv, int kvh, int hg, int j, int qrows) {
     const int i = hg * qrows + j;

@@ -63,17 +63,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // --------------------------------------------------------------------- TMA
-// 4-D tiled tensor load into CTA shared memory, completion counted in bytes
-// on an mbarrier.  Coordinates are element indices, innermost first.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0,
-                                            int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-        : "memory");
-}
-
 // L2 policy for data read exactly once (evicted first).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;
@@ -81,7 +70,9 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return pol;
 }
 
-// 5-D tiled tensor load with an L2 cache policy (same completion mechanism).
+// 5-D tiled tensor load into CTA shared memory with an L2 cache policy;
+// completion counted in bytes on an mbarrier.  Coordinates are element
+// indices, innermost first.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0,
                                             int c1, int c2, int c3, int c4, uint64_t policy) {
     asm volatile(
