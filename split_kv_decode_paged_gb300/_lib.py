@@ -1,8 +1,9 @@
 """ctypes binding of libfd.so (include/fd_api.h).  Argument marshalling only.
 
-The functions keep the C names: fd_plan, fd_decode_paged, fd_merge_states,
-fd_append_kv, fd_status_string, fd_status_from_device.  Tensors are passed
-by data_ptr(); the stream is torch's current CUDA stream unless given.  No
+Each function keeps the name of the C entry point it calls (fd_plan,
+fd_decode_paged, fd_decode_paged_ex, fd_decode_paged_host, fd_merge_states,
+fd_merge_two, fd_append_kv, fd_append_kv_rotary, ...).  Tensors are passed by
+data_ptr(); the stream is torch's current CUDA stream unless given.  No
 computation happens here and there is no fallback: if libfd.so is missing or
 fails to load, every call raises.
 """
@@ -20,10 +21,6 @@ FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE_TOO_SMALL = 0, 1
 FD_ERR_BAD_PAGE, FD_ERR_CUDA, FD_ERR_CAPACITY, FD_ERR_TIMEOUT = 4, 5, 6, 7
 FD_DEV_BAD_PAGE, FD_DEV_CAPACITY, FD_DEV_TIMEOUT = 0x1, 0x2, 0x4
 FD_F16, FD_BF16, FD_E4M3, FD_F32 = 0, 1, 2, 3
-
-EXPORTS = ("fd_plan", "fd_decode_paged", "fd_decode_paged_ex", "fd_merge_states", "fd_append_kv",
-           "fd_append_kv_rotary", "fd_merge_two", "fd_status_string", "fd_status_from_device",
-           "fd_api_version")
 
 _TORCH_TO_FD = {torch.float16: FD_F16, torch.bfloat16: FD_BF16, torch.float8_e4m3fn: FD_E4M3,
                 torch.float32: FD_F32}
