@@ -411,6 +411,7 @@ def bench_append(args):
     every call."""
     from split_kv_decode_paged_gb300 import workloads as W
     import split_kv_decode_paged_gb300 as fd
+    from split_kv_decode_paged_gb300 import _lib
     from split_kv_decode_paged_gb300 import build as fd_build
     fd_build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -440,6 +441,28 @@ def bench_append(args):
         cases[f"config {c}"] = {"workload": f"{spec.name}: B={B}, Hkv={Hkv}, D={D}, {spec.kv} pages of {spec.page_size}",
                                 "us_median": med, "us_p10": p10, "us_p90": p90, "bytes": nbytes,
                                 "gbs": nbytes / med / 1e3}
+        # The same append with rotary embedding fused in: K rotated before the
+        # cache write and q [B, Hq, D] rotated in place (GPT-NeoX pairs, the
+        # full head dimension), cos/sin tables for every position of the pool.
+        max_pos = wl.max_blocks * spec.page_size
+        ang = (torch.arange(max_pos, dtype=torch.float64)[:, None] *
+               (10000.0 ** (-torch.arange(D // 2, dtype=torch.float64) * 2 / D))[None, :])
+        cos, sin = ang.cos().float().to(dev), ang.sin().float().to(dev)
+        prob = _lib.make_problem(B, spec.Hq, Hkv, D, spec.page_size, wl.max_blocks, wl.num_pages, wl.q.dtype,
+                                 wl.k_pages.dtype)
+
+        def run_rot():
+            _lib.fd_append_kv_rotary(prob, k_new, v_new, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale,
+                                     wl.block_table, pos, cos, sin, interleaved=False, q_inout=wl.q, status=status)
+
+        med, p10, p90 = _time_flushed(run_rot, args.steps, args.warmup, flush)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"rotary append flagged status {int(status.item())}")
+        qb = 2 * B * spec.Hq * D * wl.q.element_size()
+        nb_rot = nbytes + qb + 2 * B * (D // 2) * 4 * 2  # + q read and written, cos/sin rows read
+        cases[f"config {c} rotary"] = {"workload": f"rotary append, q rotated in place (Hq={spec.Hq})",
+                                       "us_median": med, "us_p10": p10, "us_p90": p90, "bytes": nb_rot,
+                                       "gbs": nb_rot / med / 1e3}
         del wl
         torch.cuda.empty_cache()
     head = cases["config 3"]
@@ -449,6 +472,73 @@ def bench_append(args):
         "dtype": "bf16 / e4m3", "data": "synthetic", "cases": cases, "peak": peak, "peak_source": kind,
         "config": {"workload": "append one token per sequence into the GQA-batch and FP8-batch pools",
                    "l2": "flushed before every timed call (write, then read, of 256 MB)"},
+        "gpu_launches_per_call": 1}))
+
+
+def bench_ex(args):
+    """fd_decode_paged_ex on the GQA batch: q rows reach their cache rows
+    through a permuted cache_batch_idx and attend [leftpad, seq_len) with a
+    random left padding of up to a quarter of each length; against the plain
+    call on the same pools (both back to back, one event pair)."""
+    from split_kv_decode_paged_gb300 import workloads as W
+    import split_kv_decode_paged_gb300 as fd
+    from split_kv_decode_paged_gb300 import _lib
+    from split_kv_decode_paged_gb300 import build as fd_build
+    fd_build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = W.make_config(3, dev)
+    spec = wl.spec
+    B = spec.B
+    g = torch.Generator().manual_seed(303)
+    bidx = torch.randperm(B, generator=g).to(torch.int32)
+    lens = wl.seq_lens.cpu()
+    lpad = (torch.rand(B, generator=g) * (lens.float() / 4)).to(torch.int32)
+    attended = (lens[bidx.long()] - lpad[bidx.long()]).clamp(min=0)
+    dec = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, lens)
+    plan_ex = _lib.fd_plan(dec.problem, attended)
+    ws = torch.zeros(max(256, plan_ex.workspace_bytes), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(wl.q)
+    lse = torch.empty((B, spec.Hq), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bidx_d, lpad_d = bidx.to(dev), lpad.to(dev)
+
+    def run_ex():
+        _lib.fd_decode_paged_ex(plan_ex, wl.q, wl.k_pages, wl.v_pages, None, None, wl.block_table, wl.seq_lens,
+                                out, lse, ws, cache_batch_idx=bidx_d, cache_leftpad=lpad_d, cache_rows=B,
+                                status=status)
+
+    def run_plain():
+        dec(wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens, out=out, lse=lse)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("fd_timed")
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        return a.elapsed_time(b) * 1e3 / args.steps
+
+    us_ex, us_plain = timed(run_ex), timed(run_plain)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"decode_paged_ex flagged status {int(status.item())}")
+    dec.check()
+    nbytes = W.algorithmic_bytes(spec, attended) + 8 * B  # + the index and padding arrays
+    peak, kind = measured_peak()
+    print(json.dumps({
+        "metric": "fd_decode_paged_ex achieved HBM GB/s", "value": nbytes / us_ex / 1e3, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "us_per_call": us_ex,
+        "plain_decode_us_per_call": us_plain, "plain_decode_gbs": W.algorithmic_bytes(spec, lens) / us_plain / 1e3,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "bytes": nbytes, "frac_of_peak":
+        nbytes / us_ex / 1e3 / peak, "peak": peak, "peak_source": kind,
+        "config": {"workload": "GQA batch (B=64, Hq=32, Hkv=8, D=128, bf16, 16-token pages) with a permuted "
+                               "cache_batch_idx and left padding up to a quarter of each length (seed 303)",
+                   "l2": "inputs > 2x L2: back to back, one event pair"},
         "gpu_launches_per_call": 1}))
 
 
@@ -496,9 +586,10 @@ def main():
     ap.add_argument("--all-configs", action="store_true", help="also report every workload (per_config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge"],
-                    help="cascade: shared-prefix batch, cascade vs plain decode; append: fd_append_kv; "
-                         "merge: fd_merge_states")
+    ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge", "ex"],
+                    help="cascade: shared-prefix batch, cascade vs plain decode; append: fd_append_kv (plain "
+                         "and rotary); merge: fd_merge_states; ex: fd_decode_paged_ex with cache_batch_idx "
+                         "and left padding")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed decode calls (no warm-L2/graph/e2e extras, no CPU baseline)")
     args = ap.parse_args()
@@ -509,7 +600,7 @@ def main():
             print(json.dumps({"impl": "reference",
                               "unavailable": f"the {args.workload} workload is measured on the GPU path only"}))
             return
-        {"cascade": bench_cascade, "append": bench_append, "merge": bench_merge}[args.workload](args)
+        {"cascade": bench_cascade, "append": bench_append, "merge": bench_merge, "ex": bench_ex}[args.workload](args)
         return
     from split_kv_decode_paged_gb300 import workloads as W
     ws, rank, local = dist_env()
