@@ -696,7 +696,7 @@ def main():
         "us_p90": None if big else srt[(len(srt) * 9) // 10] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3 (f16 MMA, fp32 accumulate)"}[spec.kv],
-        "data": "synthetic (seeded; see DESIGN.md input recipe)", "config": config,
+        "data": "synthetic (seeded generator: split_kv_decode_paged_gb300/workloads.py)", "config": config,
         "algorithmic_bytes_per_call": bytes_call,
         "plan": {"num_splits": plan.num_splits, "chunk_tokens": plan.chunk_tokens, "grid_ctas": plan.grid_ctas,
                  "stages": plan.stages, "work_items": plan.work_items_hint, "fuse_merge": plan.fuse_merge},
