@@ -687,94 +687,109 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
         }
 
+        // The warp's SUBT sub-tiles of 16 tokens (tile rows r0 .. r0+15 with
+        // r0 = (warp*SUBT + sub)*16, each inside box r0 / boxr) share one
+        // online-softmax step: scores of every sub-tile, one check of the
+        // reference maxima (and, when needed, one reduction and O rescale),
+        // then P.V of every sub-tile.  Valid rows of a sub-tile: [ll, nl).
+        int nl[SUBT], ll[SUBT];
+        bool any_act = false;
 #pragma unroll
         for (int sub = 0; sub < SUBT; ++sub) {
-        // This warp's 16 tokens: tile rows r0 .. r0+15, inside box r0 / boxr
-        // (boxes hold NHALF swizzled regions of boxr rows x SUBROW bytes).
-        const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
-        // Valid rows of this sub-tile: [lo_loc, nloc) (lo_loc > 0 only at the
-        // start of an item that begins inside a box).
-        const int nloc = max(0, min(kTokensPerWarp, nvalid - r0));
-        const int lo_loc = max(0, vlo - r0);
-        if (nloc > lo_loc) {
-            const int rib = r0 % p.boxr;  // first row inside the box (multiple of 16)
+            const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+            nl[sub] = max(0, min(kTokensPerWarp, nvalid - r0));
+            ll[sub] = max(0, vlo - r0);
+            any_act |= nl[sub] > ll[sub];
+        }
+        if (any_act) {
             const uint32_t hstride = (uint32_t)(p.boxr * SUBROW);
-            const uint32_t box_off = (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
-            const uint32_t kbox = kbase + box_off, vbox = vbase + box_off;
-            const int row_a = rib + (lane & 7) + ((lane >> 3) & 1) * 8;  // QK: ldmatrix rows
-            const int row_t = rib + (lane & 7) + (lane >> 4) * 8;        // PV (f16/bf16): .trans rows
             // ---------------------------------------------------------- S = K Q^T
-            // Two independent accumulator chains (even / odd k-steps) halve
-            // the dependent MMA latency of the dot products.
-            float sacc[NT][4], sacc2[NT][4];
+            // Two independent accumulator chains per sub-tile (even / odd
+            // k-steps) halve the dependent MMA latency of the dot products.
+            float sv[SUBT][NT][4];
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
+            for (int sub = 0; sub < SUBT; ++sub) {
+                const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+                const uint32_t kbox = kbase + (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
+                const int row_a = r0 % p.boxr + (lane & 7) + ((lane >> 3) & 1) * 8;
+                float s2[NT][4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) sacc[n][r] = sacc2[n][r] = 0.f;
-            if constexpr (!FP8) {
+                for (int n = 0; n < NT; ++n)
 #pragma unroll
-                for (int kk = 0; kk < KT; ++kk) {
-                    const int byte = kk * 32;
-                    const int h = byte / SUBROW;
-                    const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), a0, a1, a2, a3);
+                    for (int r = 0; r < 4; ++r) sv[sub][n][r] = s2[n][r] = 0.f;
+                if (nl[sub] > ll[sub]) {
+                    if constexpr (!FP8) {
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        float *acc = (kk & 1) ? sacc2[n] : sacc[n];
-                        if constexpr (KV == KV_BF16)
-                            mma_bf16(acc, a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
-                        else
-                            mma_f16(acc, a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                        for (int kk = 0; kk < KT; ++kk) {
+                            const int byte = kk * 32;
+                            const int h = byte / SUBROW;
+                            const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), a0, a1, a2, a3);
+#pragma unroll
+                            for (int n = 0; n < NT; ++n) {
+                                float *acc = (kk & 1) ? s2[n] : sv[sub][n];
+                                if constexpr (KV == KV_BF16)
+                                    mma_bf16(acc, a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                                else
+                                    mma_f16(acc, a0, a1, a2, a3, qf[kk][n][0], qf[kk][n][1]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int jg = 0; jg < D / 32; ++jg) {
+                            const int byte = jg * 32;
+                            const int h = byte / SUBROW;
+                            const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
+                            uint32_t q0, q1, q2, q3;
+                            ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
+                            const uint32_t a00 = e4m3x2_to_f16x2((uint16_t)(q0 & 0xffff));
+                            const uint32_t a01 = e4m3x2_to_f16x2((uint16_t)(q1 & 0xffff));
+                            const uint32_t a02 = e4m3x2_to_f16x2((uint16_t)(q0 >> 16));
+                            const uint32_t a03 = e4m3x2_to_f16x2((uint16_t)(q1 >> 16));
+                            const uint32_t a10 = e4m3x2_to_f16x2((uint16_t)(q2 & 0xffff));
+                            const uint32_t a11 = e4m3x2_to_f16x2((uint16_t)(q3 & 0xffff));
+                            const uint32_t a12 = e4m3x2_to_f16x2((uint16_t)(q2 >> 16));
+                            const uint32_t a13 = e4m3x2_to_f16x2((uint16_t)(q3 >> 16));
+#pragma unroll
+                            for (int n = 0; n < NT; ++n) {
+                                mma_f16(sv[sub][n], a00, a01, a02, a03, qf[2 * jg][n][0], qf[2 * jg][n][1]);
+                                mma_f16(s2[n], a10, a11, a12, a13, qf[2 * jg + 1][n][0], qf[2 * jg + 1][n][1]);
+                            }
+                        }
                     }
                 }
-            } else {
+                // scaled, masked scores
+                float sc = scale_log2;
+                if constexpr (FP8) sc *= mt.kscale[r0 / p.boxr];
+                const bool v0 = g >= ll[sub] && g < nl[sub], v1 = (g + 8) >= ll[sub] && (g + 8) < nl[sub];
 #pragma unroll
-                for (int jg = 0; jg < D / 32; ++jg) {
-                    const int byte = jg * 32;
-                    const int h = byte / SUBROW;
-                    const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
-                    uint32_t q0, q1, q2, q3;
-                    ldsm_x4(kbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
-                    const uint32_t a00 = e4m3x2_to_f16x2((uint16_t)(q0 & 0xffff));
-                    const uint32_t a01 = e4m3x2_to_f16x2((uint16_t)(q1 & 0xffff));
-                    const uint32_t a02 = e4m3x2_to_f16x2((uint16_t)(q0 >> 16));
-                    const uint32_t a03 = e4m3x2_to_f16x2((uint16_t)(q1 >> 16));
-                    const uint32_t a10 = e4m3x2_to_f16x2((uint16_t)(q2 & 0xffff));
-                    const uint32_t a11 = e4m3x2_to_f16x2((uint16_t)(q3 & 0xffff));
-                    const uint32_t a12 = e4m3x2_to_f16x2((uint16_t)(q2 >> 16));
-                    const uint32_t a13 = e4m3x2_to_f16x2((uint16_t)(q3 >> 16));
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        mma_f16(sacc[n], a00, a01, a02, a03, qf[2 * jg][n][0], qf[2 * jg][n][1]);
-                        mma_f16(sacc2[n], a10, a11, a12, a13, qf[2 * jg + 1][n][0], qf[2 * jg + 1][n][1]);
-                    }
+                for (int n = 0; n < NT; ++n) {
+                    sv[sub][n][0] = v0 ? (sv[sub][n][0] + s2[n][0]) * sc : -INFINITY;
+                    sv[sub][n][1] = v0 ? (sv[sub][n][1] + s2[n][1]) * sc : -INFINITY;
+                    sv[sub][n][2] = v1 ? (sv[sub][n][2] + s2[n][2]) * sc : -INFINITY;
+                    sv[sub][n][3] = v1 ? (sv[sub][n][3] + s2[n][3]) * sc : -INFINITY;
                 }
             }
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) sacc[n][r] += sacc2[n][r];
 
             // ------------------------------------------------- online softmax (exp2)
-            float sc = scale_log2;
-            if constexpr (FP8) sc *= mt.kscale[r0 / p.boxr];
-            const bool v0 = g >= lo_loc && g < nloc, v1 = (g + 8) >= lo_loc && (g + 8) < nloc;
-            // Scaled, masked scores.  The reference maximum mrow only moves
-            // when some score exceeds it by more than kMaxSlack (log2 units):
-            // softmax does not depend on the reference, and the weights stay
-            // <= 2^kMaxSlack.  Then the warp reduces the tile's row maxima
-            // (three shuffle rounds) and rescales; otherwise it skips both.
-            float sv[NT][4];
+            // The reference maximum mrow only moves when some score exceeds it
+            // by more than kMaxSlack (log2 units): softmax does not depend on
+            // the reference, and the weights stay <= 2^kMaxSlack.  Then the
+            // warp reduces the step's row maxima (three shuffle rounds) and
+            // rescales; otherwise it skips both.
+            float mx[NT][2];
             bool need = false;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                sv[n][0] = v0 ? sacc[n][0] * sc : -INFINITY;
-                sv[n][1] = v0 ? sacc[n][1] * sc : -INFINITY;
-                sv[n][2] = v1 ? sacc[n][2] * sc : -INFINITY;
-                sv[n][3] = v1 ? sacc[n][3] * sc : -INFINITY;
-                need |= fmaxf(sv[n][0], sv[n][2]) > mrow[n][0] + kMaxSlack;
-                need |= fmaxf(sv[n][1], sv[n][3]) > mrow[n][1] + kMaxSlack;
+                mx[n][0] = mx[n][1] = -INFINITY;
+#pragma unroll
+                for (int sub = 0; sub < SUBT; ++sub) {
+                    mx[n][0] = fmaxf(mx[n][0], fmaxf(sv[sub][n][0], sv[sub][n][2]));
+                    mx[n][1] = fmaxf(mx[n][1], fmaxf(sv[sub][n][1], sv[sub][n][3]));
+                }
+                need |= mx[n][0] > mrow[n][0] + kMaxSlack;
+                need |= mx[n][1] > mrow[n][1] + kMaxSlack;
             }
             float alpha[NT][2];
             const bool moved = __any_sync(0xffffffffu, need);
@@ -782,56 +797,60 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             for (int n = 0; n < NT; ++n) {
                 alpha[n][0] = alpha[n][1] = 1.f;
                 if (moved) {
-                    float mx0 = fmaxf(sv[n][0], sv[n][2]), mx1 = fmaxf(sv[n][1], sv[n][3]);
 #pragma unroll
                     for (int off = 4; off < 32; off <<= 1) {
-                        mx0 = fmaxf(mx0, shfl_xor(mx0, off));
-                        mx1 = fmaxf(mx1, shfl_xor(mx1, off));
+                        mx[n][0] = fmaxf(mx[n][0], shfl_xor(mx[n][0], off));
+                        mx[n][1] = fmaxf(mx[n][1], shfl_xor(mx[n][1], off));
                     }
-                    const float mn0 = fmaxf(mrow[n][0], mx0), mn1 = fmaxf(mrow[n][1], mx1);
+                    const float mn0 = fmaxf(mrow[n][0], mx[n][0]), mn1 = fmaxf(mrow[n][1], mx[n][1]);
                     alpha[n][0] = (mn0 == -INFINITY) ? 1.f : ex2(mrow[n][0] - mn0);
                     alpha[n][1] = (mn1 == -INFINITY) ? 1.f : ex2(mrow[n][1] - mn1);
                     mrow[n][0] = mn0;
                     mrow[n][1] = mn1;
                 }
             }
-            uint32_t pb[NT][2];
-            uint32_t pl[NT][2];  // bf16 V: low parts of the weights (P = hi + lo)
+            uint32_t pb[SUBT][NT][2];
+            uint32_t pl[SUBT][NT][2];  // bf16 V: low parts of the weights (P = hi + lo)
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 const float mn0 = mrow[n][0], mn1 = mrow[n][1];
-                const float s0 = sv[n][0], s1 = sv[n][1], s2 = sv[n][2], s3 = sv[n][3];
-                const float p0 = (mn0 == -INFINITY) ? 0.f : ex2(s0 - mn0);
-                const float p1 = (mn1 == -INFINITY) ? 0.f : ex2(s1 - mn1);
-                const float p2 = (mn0 == -INFINITY) ? 0.f : ex2(s2 - mn0);
-                const float p3 = (mn1 == -INFINITY) ? 0.f : ex2(s3 - mn1);
-                uint32_t x0, x1;
-                float wr0, wr1, wr2, wr3;  // the rounded weights actually used
-                if constexpr (KV == KV_BF16) {
-                    // bf16 keeps 8 significant bits; the weights enter P.V as
-                    // hi + lo bf16 pairs (two MMAs on one V fragment), so the
-                    // product sees them to ~2^-17 relative.
-                    x0 = pack_bf16x2(p0, p1);
-                    x1 = pack_bf16x2(p2, p3);
-                    const float h0 = __uint_as_float(x0 << 16), h1 = __uint_as_float(x0 & 0xffff0000u);
-                    const float h2 = __uint_as_float(x1 << 16), h3 = __uint_as_float(x1 & 0xffff0000u);
-                    const uint32_t y0 = pack_bf16x2(p0 - h0, p1 - h1);
-                    const uint32_t y1 = pack_bf16x2(p2 - h2, p3 - h3);
-                    wr0 = h0 + __uint_as_float(y0 << 16); wr1 = h1 + __uint_as_float(y0 & 0xffff0000u);
-                    wr2 = h2 + __uint_as_float(y1 << 16); wr3 = h3 + __uint_as_float(y1 & 0xffff0000u);
-                    pl[n][0] = movmatrix_t(y0);
-                    pl[n][1] = movmatrix_t(y1);
-                } else {
-                    x0 = pack_f16x2(p0, p1);
-                    x1 = pack_f16x2(p2, p3);
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&x0));
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&x1));
-                    wr0 = f0.x; wr1 = f0.y; wr2 = f1.x; wr3 = f1.y;
+                float add0 = 0.f, add1 = 0.f;
+#pragma unroll
+                for (int sub = 0; sub < SUBT; ++sub) {
+                    const float p0 = (mn0 == -INFINITY) ? 0.f : ex2(sv[sub][n][0] - mn0);
+                    const float p1 = (mn1 == -INFINITY) ? 0.f : ex2(sv[sub][n][1] - mn1);
+                    const float p2 = (mn0 == -INFINITY) ? 0.f : ex2(sv[sub][n][2] - mn0);
+                    const float p3 = (mn1 == -INFINITY) ? 0.f : ex2(sv[sub][n][3] - mn1);
+                    uint32_t x0, x1;
+                    float wr0, wr1, wr2, wr3;  // the rounded weights actually used
+                    if constexpr (KV == KV_BF16) {
+                        // bf16 keeps 8 significant bits; the weights enter P.V
+                        // as hi + lo bf16 pairs (two MMAs on one V fragment),
+                        // so the product sees them to ~2^-17 relative.
+                        x0 = pack_bf16x2(p0, p1);
+                        x1 = pack_bf16x2(p2, p3);
+                        const float h0 = __uint_as_float(x0 << 16), h1 = __uint_as_float(x0 & 0xffff0000u);
+                        const float h2 = __uint_as_float(x1 << 16), h3 = __uint_as_float(x1 & 0xffff0000u);
+                        const uint32_t y0 = pack_bf16x2(p0 - h0, p1 - h1);
+                        const uint32_t y1 = pack_bf16x2(p2 - h2, p3 - h3);
+                        wr0 = h0 + __uint_as_float(y0 << 16); wr1 = h1 + __uint_as_float(y0 & 0xffff0000u);
+                        wr2 = h2 + __uint_as_float(y1 << 16); wr3 = h3 + __uint_as_float(y1 & 0xffff0000u);
+                        pl[sub][n][0] = movmatrix_t(y0);
+                        pl[sub][n][1] = movmatrix_t(y1);
+                    } else {
+                        x0 = pack_f16x2(p0, p1);
+                        x1 = pack_f16x2(p2, p3);
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&x0));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&x1));
+                        wr0 = f0.x; wr1 = f0.y; wr2 = f1.x; wr3 = f1.y;
+                    }
+                    add0 += wr0 + wr2;
+                    add1 += wr1 + wr3;
+                    pb[sub][n][0] = movmatrix_t(x0);
+                    pb[sub][n][1] = movmatrix_t(x1);
                 }
-                lrow[n][0] = lrow[n][0] * alpha[n][0] + (wr0 + wr2);
-                lrow[n][1] = lrow[n][1] * alpha[n][1] + (wr1 + wr3);
-                pb[n][0] = movmatrix_t(x0);
-                pb[n][1] = movmatrix_t(x1);
+                lrow[n][0] = lrow[n][0] * alpha[n][0] + add0;
+                lrow[n][1] = lrow[n][1] * alpha[n][1] + add1;
             }
             if (moved) {
 #pragma unroll
@@ -846,73 +865,82 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
 
             // ---------------------------------------------------- O^T += V^T P^T
-            // Rows outside [lo_loc, nloc) may hold any bits (stale or NaN):
-            // partial sub-tiles zero their V fragments.
-            const bool part = nloc < kTokensPerWarp || lo_loc > 0;
-            uint32_t msk01 = 0xffffffffu, msk23 = 0xffffffffu;
-            if (part) {
-                auto ok_t = [&](int t) { return t >= lo_loc && t < nloc; };
-                msk01 = (ok_t(2 * c) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 1) ? 0xffff0000u : 0u);
-                msk23 = (ok_t(2 * c + 8) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 9) ? 0xffff0000u : 0u);
-            }
-            if constexpr (!FP8) {
 #pragma unroll
-                for (int mi = 0; mi < MT; ++mi) {
-                    const int byte = mi * 32;
-                    const int h = byte / SUBROW;
-                    const int chunk = (byte % SUBROW) / 16 + ((lane >> 3) & 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_t, chunk), a0, a1, a2, a3);
-                    if (part) { a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23; }
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        if constexpr (KV == KV_BF16) {
-                            mma_bf16(o[mi][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
-                            mma_bf16(o[mi][n], a0, a1, a2, a3, pl[n][0], pl[n][1]);
-                        } else {
-                            mma_f16(o[mi][n], a0, a1, a2, a3, pb[n][0], pb[n][1]);
-                        }
-                    }
+            for (int sub = 0; sub < SUBT; ++sub) {
+                if (!(nl[sub] > ll[sub])) continue;
+                const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+                const int rib = r0 % p.boxr;
+                const uint32_t vbox = vbase + (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
+                // Rows outside [ll, nl) may hold any bits (stale or NaN):
+                // partial sub-tiles zero their V fragments.
+                const bool part = nl[sub] < kTokensPerWarp || ll[sub] > 0;
+                uint32_t msk01 = 0xffffffffu, msk23 = 0xffffffffu;
+                if (part) {
+                    const int lo_t = ll[sub], hi_t = nl[sub];
+                    auto ok_t = [&](int t) { return t >= lo_t && t < hi_t; };
+                    msk01 = (ok_t(2 * c) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 1) ? 0xffff0000u : 0u);
+                    msk23 = (ok_t(2 * c + 8) ? 0x0000ffffu : 0u) | (ok_t(2 * c + 9) ? 0xffff0000u : 0u);
                 }
-            } else {
-                const float vsc = mt.vscale[r0 / p.boxr];
+                if constexpr (!FP8) {
+                    const int row_t = rib + (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-                for (int jg = 0; jg < D / 32; ++jg) {
-                    const int byte = jg * 32;
-                    const int h = byte / SUBROW;
-                    const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
-                    uint32_t q0, q1, q2, q3;
-                    ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
-                    // the 16-bit halves of q0, q2 hold tokens 2c, 2c+1; of q1,
-                    // q3 tokens 2c+8, 2c+9 (E4M3 zero bytes convert to +0)
-                    if (part) { q0 &= msk01; q1 &= msk23; q2 &= msk01; q3 &= msk23; }
-                    const uint32_t t0 = __byte_perm(q0, 0, 0x3120), t1 = __byte_perm(q1, 0, 0x3120);
-                    const uint32_t t2 = __byte_perm(q2, 0, 0x3120), t3 = __byte_perm(q3, 0, 0x3120);
-                    uint32_t A[2][4];
-                    A[0][0] = e4m3x2_to_f16x2((uint16_t)(t0 & 0xffff));
-                    A[0][1] = e4m3x2_to_f16x2((uint16_t)(t0 >> 16));
-                    A[0][2] = e4m3x2_to_f16x2((uint16_t)(t1 & 0xffff));
-                    A[0][3] = e4m3x2_to_f16x2((uint16_t)(t1 >> 16));
-                    A[1][0] = e4m3x2_to_f16x2((uint16_t)(t2 & 0xffff));
-                    A[1][1] = e4m3x2_to_f16x2((uint16_t)(t2 >> 16));
-                    A[1][2] = e4m3x2_to_f16x2((uint16_t)(t3 & 0xffff));
-                    A[1][3] = e4m3x2_to_f16x2((uint16_t)(t3 >> 16));
-#pragma unroll
-                    for (int hs = 0; hs < 2; ++hs)
+                    for (int mi = 0; mi < MT; ++mi) {
+                        const int byte = mi * 32;
+                        const int h = byte / SUBROW;
+                        const int chunk = (byte % SUBROW) / 16 + ((lane >> 3) & 1);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_t, chunk), a0, a1, a2, a3);
+                        if (part) { a0 &= msk01; a1 &= msk01; a2 &= msk23; a3 &= msk23; }
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
-                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_f16(acc, A[hs][0], A[hs][1], A[hs][2], A[hs][3], pb[n][0], pb[n][1]);
-                            float *od = o[2 * jg + hs][n];
-                            od[0] = fmaf(acc[0], vsc, od[0]);
-                            od[1] = fmaf(acc[1], vsc, od[1]);
-                            od[2] = fmaf(acc[2], vsc, od[2]);
-                            od[3] = fmaf(acc[3], vsc, od[3]);
+                            if constexpr (KV == KV_BF16) {
+                                mma_bf16(o[mi][n], a0, a1, a2, a3, pb[sub][n][0], pb[sub][n][1]);
+                                mma_bf16(o[mi][n], a0, a1, a2, a3, pl[sub][n][0], pl[sub][n][1]);
+                            } else {
+                                mma_f16(o[mi][n], a0, a1, a2, a3, pb[sub][n][0], pb[sub][n][1]);
+                            }
                         }
+                    }
+                } else {
+                    const int row_a = rib + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const float vsc = mt.vscale[r0 / p.boxr];
+#pragma unroll
+                    for (int jg = 0; jg < D / 32; ++jg) {
+                        const int byte = jg * 32;
+                        const int h = byte / SUBROW;
+                        const int chunk = (byte % SUBROW) / 16 + (lane >> 4);
+                        uint32_t q0, q1, q2, q3;
+                        ldsm_x4_t(vbox + (uint32_t)h * hstride + swz<SUBROW>(row_a, chunk), q0, q1, q2, q3);
+                        // the 16-bit halves of q0, q2 hold tokens 2c, 2c+1; of
+                        // q1, q3 tokens 2c+8, 2c+9 (E4M3 zero bytes convert to +0)
+                        if (part) { q0 &= msk01; q1 &= msk23; q2 &= msk01; q3 &= msk23; }
+                        const uint32_t t0 = __byte_perm(q0, 0, 0x3120), t1 = __byte_perm(q1, 0, 0x3120);
+                        const uint32_t t2 = __byte_perm(q2, 0, 0x3120), t3 = __byte_perm(q3, 0, 0x3120);
+                        uint32_t A[2][4];
+                        A[0][0] = e4m3x2_to_f16x2((uint16_t)(t0 & 0xffff));
+                        A[0][1] = e4m3x2_to_f16x2((uint16_t)(t0 >> 16));
+                        A[0][2] = e4m3x2_to_f16x2((uint16_t)(t1 & 0xffff));
+                        A[0][3] = e4m3x2_to_f16x2((uint16_t)(t1 >> 16));
+                        A[1][0] = e4m3x2_to_f16x2((uint16_t)(t2 & 0xffff));
+                        A[1][1] = e4m3x2_to_f16x2((uint16_t)(t2 >> 16));
+                        A[1][2] = e4m3x2_to_f16x2((uint16_t)(t3 & 0xffff));
+                        A[1][3] = e4m3x2_to_f16x2((uint16_t)(t3 >> 16));
+#pragma unroll
+                        for (int hs = 0; hs < 2; ++hs)
+#pragma unroll
+                            for (int n = 0; n < NT; ++n) {
+                                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_f16(acc, A[hs][0], A[hs][1], A[hs][2], A[hs][3], pb[sub][n][0], pb[sub][n][1]);
+                                float *od = o[2 * jg + hs][n];
+                                od[0] = fmaf(acc[0], vsc, od[0]);
+                                od[1] = fmaf(acc[1], vsc, od[1]);
+                                od[2] = fmaf(acc[2], vsc, od[2]);
+                                od[3] = fmaf(acc[3], vsc, od[3]);
+                            }
+                    }
                 }
             }
         }
-        }  // sub-tiles
         // Release the stage (all reads of it are done).
         const int m_kvh = mt.kvh, m_s = mt.s, m_nsplit = mt.nsplit, m_hg = mt.hg, m_nrows = mt.nrows;
         __syncwarp();
