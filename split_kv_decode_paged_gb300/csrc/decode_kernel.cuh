@@ -90,6 +90,20 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
         return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
+// Lanes of the warp whose 7-bit key equals this lane's (what match.any
+// returns), from one ballot per key bit: a fixed cost whatever the number of
+// distinct keys in the warp.
+__device__ __forceinline__ unsigned same_key_lanes(unsigned key) {
+    unsigned m = 0xffffffffu;
+#pragma unroll
+    for (int bit = 0; bit < 7; ++bit) {
+        const bool set = (key >> bit) & 1u;
+        const unsigned v = __ballot_sync(0xffffffffu, set);
+        m &= set ? v : ~v;
+    }
+    return m;
+}
+
 __device__ __forceinline__ void flag_status(int *status, int bit) {
     if (status) atomicOr(status, bit);
 }
@@ -281,17 +295,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // K/V are streamed once per call: keep them from displacing other lines in L2.
         const uint64_t kv_policy = l2_policy_evict_first();
         const int BPT = TILE / boxr;  // boxes per tile: 1, 2, 4 (or 8)
-        // Cache row of q row b (block table, seq_lens and leftpad are
-        // indexed by it); -1 for an index outside the cache (flagged).
-        auto cache_row = [&](int b) -> int {
-            if (!p.batch_idx) return b;
-            const int cb = __ldg(p.batch_idx + b);
-            if (cb < 0 || cb >= p.cache_rows) {
-                flag_status(p.status, FD_DEV_BAD_PAGE);
-                return -1;
-            }
-            return cb;
-        };
+        // boxr divides the power-of-two tile, so it is a power of two itself.
+        const int bxs = __ffs(boxr) - 1;
+        const int bpp = ps >> bxs;    // boxes per page
         // Warm L2 with the block table (each CTA one slice of it) while the
         // dispatch tables are built, so the first items' page ids hit L2.
         {
@@ -309,30 +315,51 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         //     (stable counting sort into kOrderBuckets buckets).
         // Largest items go first and the smallest fill the tail.
         // Attended length of every row: tokens [leftpad, seq_len) of its cache
-        // row.  No warp collective in this loop, so its loads overlap.
-        for (int b = lane; b < B; b += 32) {
-            const int cb = cache_row(b);
-            int L = 0;
-            if (cb >= 0) {
-                L = p.seq_lens[cb];
-                if (p.leftpad) {
-                    const int lp = p.leftpad[cb];
-                    L = (lp < 0 || lp > L) ? -1 : L - lp;
+        // row (block table, seq_lens and leftpad are indexed by the cache row;
+        // an index outside the cache is flagged and the row attends nothing).
+        // Four rows per lane per round, every load issued before any is used,
+        // so a round costs one memory latency.
+        for (int b0 = 0; b0 < B; b0 += 4 * 32) {
+            int cbv[4], slv[4], lpv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * 32 + lane;
+                cbv[u] = b >= B ? -1 : (p.batch_idx ? __ldg(p.batch_idx + b) : b);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = cbv[u] >= 0 && cbv[u] < p.cache_rows;
+                slv[u] = in ? __ldg(p.seq_lens + cbv[u]) : 0;
+                lpv[u] = (in && p.leftpad) ? __ldg(p.leftpad + cbv[u]) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * 32 + lane;
+                if (b >= B) continue;
+                int L = 0;
+                if (cbv[u] < 0 || cbv[u] >= p.cache_rows) {
+                    flag_status(p.status, FD_DEV_BAD_PAGE);
+                } else {
+                    L = slv[u];
+                    if (p.leftpad) L = (lpv[u] < 0 || lpv[u] > L) ? -1 : L - lpv[u];
                 }
+                if (L < 0 || L > p.cap) {
+                    flag_status(p.status, FD_DEV_CAPACITY);
+                    L = L < 0 ? 0 : p.cap;
+                }
+                lens[b] = L;
             }
-            if (L < 0 || L > p.cap) {
-                flag_status(p.status, FD_DEV_CAPACITY);
-                L = L < 0 ? 0 : p.cap;
-            }
-            lens[b] = L;
         }
         for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
         __syncwarp();
-        const long long c1 = (long long)C + 1;
         auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
-        auto bucket_of = [&](int r) {
-            return (kOrderBuckets - 1) - (int)min((long long)(kOrderBuckets - 1), ((long long)r * kOrderBuckets) / c1);
-        };
+        // Bucket of a partial chunk of r < C tokens: r >> bsh < 64 for all of
+        // them (buckets 2^bsh tokens wide, C / 64 < 2^bsh <= C / 32), longer
+        // chunks in lower buckets.  A shift, not a division: this runs once
+        // per row, twice, on the path to the first load.
+        static_assert(kOrderBuckets == 64, "bucket_of assumes 64 buckets");
+        const int bsh = max(0, 26 - __clz(C));
+        auto bucket_of = [&](int r) { return (kOrderBuckets - 1) - (r >> bsh); };
         int runningA = 0;
         for (int base = 0; base < B; base += 32) {
             const int b = base + lane;
@@ -344,7 +371,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 const int r = tail_of(L);
                 if (r >= 0) bucket = bucket_of(r);
             }
-            const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+            const unsigned peers = same_key_lanes((unsigned)bucket);
             if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vA += __shfl_xor_sync(0xffffffffu, vA, o);
@@ -373,7 +400,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const int b = base + lane;
             const int r = b < B ? tail_of(lens[b]) : -1;
             const int bucket = r >= 0 ? bucket_of(r) : kOrderBuckets;
-            const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+            const unsigned peers = same_key_lanes((unsigned)bucket);
             if (bucket < kOrderBuckets) {
                 const unsigned below = peers & ((1u << lane) - 1u);
                 order[hist[bucket] + __popc(below)] = (uint16_t)b;
@@ -439,12 +466,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             it.t_begin = lp + it.s * C;
             it.t_end = lp + min(it.L, it.s * C + C);
             it.ntok = max(0, it.t_end - it.t_begin);
-            const int a = it.ntok > 0 ? (it.t_begin / boxr) * boxr : it.t_begin;
+            const int a = it.ntok > 0 ? (it.t_begin >> bxs) << bxs : it.t_begin;
             it.vlo = it.t_begin - a;
             const int span = it.ntok > 0 ? it.t_end - a : 0;
             it.ntiles = max(1, (span + TILE - 1) / TILE);
-            it.nbox = (span + boxr - 1) / boxr;
-            it.box0 = a / boxr;
+            it.nbox = (span + boxr - 1) >> bxs;
+            it.box0 = a >> bxs;
             it.t_begin = a;  // tiles are laid out from the aligned start
             return it;
         };
@@ -452,7 +479,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // column out of range).
         auto page_of = [&](const Item &it, int k) -> int {
             if (k >= it.nbox) return -1;
-            const int col = ((it.box0 + k) * boxr) / ps;
+            const int col = (it.box0 + k) / bpp;
             if (col >= p.max_blocks) return -2;
             return __ldg(p.block_table + (size_t)it.cb * p.max_blocks + col);
         };
