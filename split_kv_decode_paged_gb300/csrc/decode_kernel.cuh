@@ -44,6 +44,7 @@
 namespace fd {
 
 constexpr int kOrderBuckets = 64;  // length buckets of the partial-chunk dispatch order (2 per lane)
+constexpr int kCoopBlocks = 4;     // 32-row blocks from which every warp builds the dispatch tables
 constexpr int kFlagFirst = 1;
 constexpr int kFlagLast = 2;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -240,6 +241,156 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int n
     }
 }
 
+// Dispatch tables of a large batch (at least kCoopBlocks 32-row blocks),
+// built by all NC + 1 warps of the CTA: the consumers have nothing to do
+// before the first stage lands.  The result is the one the producer builds
+// alone for small batches (same lengths, block prefixes, bucket function and
+// stable order).  Every warp takes a contiguous run of blocks with its own
+// bucket counts: (1) lengths, per-block item counts and per-warp bucket
+// counts; (2) the last warp scans both into block prefixes (bpre[nb] = all
+// full-chunk items) and per-warp bucket offsets (hist[(NC + 1) * 64] = all
+// partial-chunk rows); (3) every warp places its rows.  hist is scratch of
+// (NC + 1) * 64 + 1 ints.  Called by every thread of the CTA (it holds CTA
+// barriers); kept out of line so the small-batch kernel body stays as it is.
+template <int NC>
+__device__ __noinline__ void build_dispatch_tables_coop(const DecodeParams &p, int *bpre, int *lens, int *hist,
+                                                        uint16_t *order, int warp, int lane) {
+    constexpr int NW = NC + 1;
+    const int Bkv = p.Bkv, C = p.chunk, HG = p.Hkv * p.nhg;  // HG: items per chunk of a KV row
+    const int nb = (Bkv + 31) >> 5;
+    const int blk0 = (warp * nb) / NW, blk1 = ((warp + 1) * nb) / NW;
+    int *hw = hist + warp * kOrderBuckets;  // this warp's bucket counts, then offsets
+    auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
+    const int bsh = max(0, 26 - __clz(C));  // as in the kernel's producer
+    auto bucket_of = [&](int r) { return (kOrderBuckets - 1) - (r >> bsh); };
+    // Warm L2 with the block table (a slice per thread of every CTA).
+    {
+        const long long bt_bytes = (long long)p.cache_rows * p.max_blocks * (long long)sizeof(int32_t);
+        if (bt_bytes <= (4 << 20)) {
+            const char *bt = reinterpret_cast<const char *>(p.block_table);
+            for (int off = ((int)blockIdx.x * 32 * NW + warp * 32 + lane) * 128; off < (int)bt_bytes;
+                 off += (int)gridDim.x * 32 * NW * 128)
+                prefetch_l2(bt + off);
+        }
+    }
+    for (int i = lane; i < kOrderBuckets; i += 32) hw[i] = 0;
+    __syncwarp();
+    // (1) Four blocks per round, every load issued before any is used.
+    for (int k0 = blk0; k0 < blk1; k0 += 4) {
+        bool row[4];
+        int cbv[4], slv[4], lpv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int b = (k0 + u) * 32 + lane;
+            row[u] = k0 + u < blk1 && b < Bkv;
+            cbv[u] = !row[u] ? -1 : (p.batch_idx ? __ldg(p.batch_idx + b) : b);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool in = row[u] && cbv[u] >= 0 && cbv[u] < p.cache_rows;
+            slv[u] = in ? __ldg(p.seq_lens + cbv[u]) : 0;
+            lpv[u] = (in && p.leftpad) ? __ldg(p.leftpad + cbv[u]) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (k0 + u >= blk1) break;  // warp-uniform
+            const int b = (k0 + u) * 32 + lane;
+            int bucket = kOrderBuckets;  // sentinel: past B or no partial chunk
+            int vA = 0;
+            if (row[u]) {
+                int L = 0;
+                if (cbv[u] < 0 || cbv[u] >= p.cache_rows) {
+                    flag_status(p.status, FD_DEV_BAD_PAGE);
+                } else {
+                    L = slv[u];
+                    if (p.leftpad) L = (lpv[u] < 0 || lpv[u] > L) ? -1 : L - lpv[u];
+                }
+                if (L < 0 || L > p.cap) {
+                    flag_status(p.status, FD_DEV_CAPACITY);
+                    L = L < 0 ? 0 : p.cap;
+                }
+                lens[b] = L;
+                vA = (L / C) * HG;
+                const int r = tail_of(L);
+                if (r >= 0) bucket = bucket_of(r);
+            }
+            const unsigned peers = same_key_lanes((unsigned)bucket);
+            if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hw[bucket] += __popc(peers);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) vA += __shfl_xor_sync(0xffffffffu, vA, o);
+            if (lane == 0) bpre[k0 + u] = vA;  // the block's item count, scanned below
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (warp == NC) {
+        // (2a) Block item counts -> exclusive prefix.
+        const int per = (nb + 31) >> 5;
+        int sum = 0;
+        for (int i = 0; i < per; ++i) {
+            const int k = lane * per + i;
+            if (k < nb) sum += bpre[k];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int run = incl - sum;
+        for (int i = 0; i < per; ++i) {
+            const int k = lane * per + i;
+            if (k < nb) {
+                const int v = bpre[k];
+                bpre[k] = run;
+                run += v;
+            }
+        }
+        if (lane == 31) bpre[nb] = incl;
+        // (2b) Bucket counts (2 buckets per lane) -> where each warp's rows
+        // of each bucket start.
+        int t0 = 0, t1 = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            t0 += hist[w * kOrderBuckets + 2 * lane];
+            t1 += hist[w * kOrderBuckets + 2 * lane + 1];
+        }
+        int v = t0 + t1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+        }
+        int r0 = v - t0 - t1, r1 = v - t1;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            int *h = hist + w * kOrderBuckets + 2 * lane;
+            const int c0 = h[0], c1 = h[1];
+            h[0] = r0;
+            h[1] = r1;
+            r0 += c0;
+            r1 += c1;
+        }
+        if (lane == 31) hist[NW * kOrderBuckets] = v;
+    }
+    __syncthreads();
+    // (3) Place this warp's rows in the partial-chunk order.
+    for (int k = blk0; k < blk1; ++k) {
+        const int b = k * 32 + lane;
+        const int r = b < Bkv ? tail_of(lens[b]) : -1;
+        const int bucket = r >= 0 ? bucket_of(r) : kOrderBuckets;
+        const unsigned peers = same_key_lanes((unsigned)bucket);
+        if (bucket < kOrderBuckets) {
+            const unsigned below = peers & ((1u << lane) - 1u);
+            order[hw[bucket] + __popc(below)] = (uint16_t)b;
+        }
+        __syncwarp();
+        if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hw[bucket] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+}
+
 template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     fd_split_kv_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
@@ -287,6 +438,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // parameters; global inputs and the workspace are read after the
     // preceding grid (e.g. the previous decode call) has completed.
     grid_dependency_wait();
+    // Large batches: every warp builds the dispatch tables (see
+    // build_dispatch_tables_coop); small ones: the producer alone, below.
+    // Shapes at the register limit (two head tiles of D = 128) keep the
+    // producer-only build: the out-of-line call would make them spill.
+    constexpr bool kCoopTables = !(NT == 2 && D == 128);
+    const bool coop = kCoopTables && ((p.Bkv + 31) >> 5) >= kCoopBlocks;  // the same in every thread
+    // Its per-warp bucket tables live in the first stage, unused until the
+    // producer issues the first load, after the tables are complete.
+    static_assert(Sh::STAGE >= ((NC + 1) * kOrderBuckets + 1) * (int)sizeof(int), "bucket tables fit in a stage");
+    int *coop_hist = reinterpret_cast<int *>(stages);  // (NC + 1) * kOrderBuckets + 1
+    if constexpr (kCoopTables)
+        if (coop) build_dispatch_tables_coop<NC>(p, bpre, lens, coop_hist, order, warp, lane);
 
     if (warp == NC) {
         // ================================================================ producer
@@ -298,118 +461,123 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // boxr divides the power-of-two tile, so it is a power of two itself.
         const int bxs = __ffs(boxr) - 1;
         const int bpp = ps >> bxs;    // boxes per page
-        // Warm L2 with the block table (each CTA one slice of it) while the
-        // dispatch tables are built, so the first items' page ids hit L2.
-        {
-            const long long bt_bytes = (long long)p.cache_rows * p.max_blocks * (long long)sizeof(int32_t);
-            if (bt_bytes <= (4 << 20)) {
-                const char *bt = reinterpret_cast<const char *>(p.block_table);
-                for (int off = ((int)blockIdx.x * 32 + lane) * 128; off < (int)bt_bytes; off += (int)gridDim.x * 32 * 128)
-                    prefetch_l2(bt + off);
-            }
-        }
-        // Dispatch order, identical in every CTA (it depends only on seq_lens):
-        //  A: every full chunk (C tokens) of every KV row, in row order;
-        //  B: the last, partial chunk of each row (or the single empty item of
-        //     an empty row), rows sorted by that chunk's length, longest first
-        //     (stable counting sort into kOrderBuckets buckets).
-        // Largest items go first and the smallest fill the tail.
-        // Attended length of every row: tokens [leftpad, seq_len) of its cache
-        // row (block table, seq_lens and leftpad are indexed by the cache row;
-        // an index outside the cache is flagged and the row attends nothing).
-        // Four rows per lane per round, every load issued before any is used,
-        // so a round costs one memory latency.
-        for (int b0 = 0; b0 < B; b0 += 4 * 32) {
-            int cbv[4], slv[4], lpv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int b = b0 + u * 32 + lane;
-                cbv[u] = b >= B ? -1 : (p.batch_idx ? __ldg(p.batch_idx + b) : b);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const bool in = cbv[u] >= 0 && cbv[u] < p.cache_rows;
-                slv[u] = in ? __ldg(p.seq_lens + cbv[u]) : 0;
-                lpv[u] = (in && p.leftpad) ? __ldg(p.leftpad + cbv[u]) : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int b = b0 + u * 32 + lane;
-                if (b >= B) continue;
-                int L = 0;
-                if (cbv[u] < 0 || cbv[u] >= p.cache_rows) {
-                    flag_status(p.status, FD_DEV_BAD_PAGE);
-                } else {
-                    L = slv[u];
-                    if (p.leftpad) L = (lpv[u] < 0 || lpv[u] > L) ? -1 : L - lpv[u];
+        int totalA = 0, nB = 0;
+        if (coop) {
+            totalA = bpre[(B + 31) >> 5];
+            nB = coop_hist[(NC + 1) * kOrderBuckets];
+        } else {
+            // Warm L2 with the block table (each CTA one slice of it) while the
+            // dispatch tables are built, so the first items' page ids hit L2.
+            {
+                const long long bt_bytes = (long long)p.cache_rows * p.max_blocks * (long long)sizeof(int32_t);
+                if (bt_bytes <= (4 << 20)) {
+                    const char *bt = reinterpret_cast<const char *>(p.block_table);
+                    for (int off = ((int)blockIdx.x * 32 + lane) * 128; off < (int)bt_bytes; off += (int)gridDim.x * 32 * 128)
+                        prefetch_l2(bt + off);
                 }
-                if (L < 0 || L > p.cap) {
-                    flag_status(p.status, FD_DEV_CAPACITY);
-                    L = L < 0 ? 0 : p.cap;
+            }
+            // Dispatch order, identical in every CTA (it depends only on seq_lens):
+            //  A: every full chunk (C tokens) of every KV row, in row order;
+            //  B: the last, partial chunk of each row (or the single empty item of
+            //     an empty row), rows sorted by that chunk's length, longest first
+            //     (stable counting sort into kOrderBuckets buckets).
+            // Largest items go first and the smallest fill the tail.
+            // Attended length of every row: tokens [leftpad, seq_len) of its cache
+            // row (block table, seq_lens and leftpad are indexed by the cache row;
+            // an index outside the cache is flagged and the row attends nothing).
+            // Four rows per lane per round, every load issued before any is used,
+            // so a round costs one memory latency.
+            for (int b0 = 0; b0 < B; b0 += 4 * 32) {
+                int cbv[4], slv[4], lpv[4];
+    #pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int b = b0 + u * 32 + lane;
+                    cbv[u] = b >= B ? -1 : (p.batch_idx ? __ldg(p.batch_idx + b) : b);
                 }
-                lens[b] = L;
+    #pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const bool in = cbv[u] >= 0 && cbv[u] < p.cache_rows;
+                    slv[u] = in ? __ldg(p.seq_lens + cbv[u]) : 0;
+                    lpv[u] = (in && p.leftpad) ? __ldg(p.leftpad + cbv[u]) : 0;
+                }
+    #pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int b = b0 + u * 32 + lane;
+                    if (b >= B) continue;
+                    int L = 0;
+                    if (cbv[u] < 0 || cbv[u] >= p.cache_rows) {
+                        flag_status(p.status, FD_DEV_BAD_PAGE);
+                    } else {
+                        L = slv[u];
+                        if (p.leftpad) L = (lpv[u] < 0 || lpv[u] > L) ? -1 : L - lpv[u];
+                    }
+                    if (L < 0 || L > p.cap) {
+                        flag_status(p.status, FD_DEV_CAPACITY);
+                        L = L < 0 ? 0 : p.cap;
+                    }
+                    lens[b] = L;
+                }
             }
-        }
-        for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
-        __syncwarp();
-        auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
-        // Bucket of a partial chunk of r < C tokens: r >> bsh < 64 for all of
-        // them (buckets 2^bsh tokens wide, C / 64 < 2^bsh <= C / 32), longer
-        // chunks in lower buckets.  A shift, not a division: this runs once
-        // per row, twice, on the path to the first load.
-        static_assert(kOrderBuckets == 64, "bucket_of assumes 64 buckets");
-        const int bsh = max(0, 26 - __clz(C));
-        auto bucket_of = [&](int r) { return (kOrderBuckets - 1) - (r >> bsh); };
-        int runningA = 0;
-        for (int base = 0; base < B; base += 32) {
-            const int b = base + lane;
-            int bucket = kOrderBuckets;  // sentinel: past B or no partial chunk
-            int vA = 0;
-            if (b < B) {
-                const int L = lens[b];
-                vA = (L / C) * HG;
-                const int r = tail_of(L);
-                if (r >= 0) bucket = bucket_of(r);
+            for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
+            __syncwarp();
+            auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
+            // Bucket of a partial chunk of r < C tokens: r >> bsh < 64 for all of
+            // them (buckets 2^bsh tokens wide, C / 64 < 2^bsh <= C / 32), longer
+            // chunks in lower buckets.  A shift, not a division: this runs once
+            // per row, twice, on the path to the first load.
+            static_assert(kOrderBuckets == 64, "bucket_of assumes 64 buckets");
+            const int bsh = max(0, 26 - __clz(C));
+            auto bucket_of = [&](int r) { return (kOrderBuckets - 1) - (r >> bsh); };
+            int runningA = 0;
+            for (int base = 0; base < B; base += 32) {
+                const int b = base + lane;
+                int bucket = kOrderBuckets;  // sentinel: past B or no partial chunk
+                int vA = 0;
+                if (b < B) {
+                    const int L = lens[b];
+                    vA = (L / C) * HG;
+                    const int r = tail_of(L);
+                    if (r >= 0) bucket = bucket_of(r);
+                }
+                const unsigned peers = same_key_lanes((unsigned)bucket);
+                if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+    #pragma unroll
+                for (int o = 16; o > 0; o >>= 1) vA += __shfl_xor_sync(0xffffffffu, vA, o);
+                if (lane == 0) bpre[base >> 5] = runningA;
+                runningA += vA;
+                __syncwarp();
             }
-            const unsigned peers = same_key_lanes((unsigned)bucket);
-            if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) vA += __shfl_xor_sync(0xffffffffu, vA, o);
-            if (lane == 0) bpre[base >> 5] = runningA;
-            runningA += vA;
-            __syncwarp();
-        }
-        if (lane == 0) bpre[(B + 31) >> 5] = runningA;
-        int nB = 0;
-        {   // exclusive scan of the bucket counts (2 buckets per lane)
-            const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
-            int v = h0 + h1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += t;
+            if (lane == 0) bpre[(B + 31) >> 5] = runningA;
+            {   // exclusive scan of the bucket counts (2 buckets per lane)
+                const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
+                int v = h0 + h1;
+    #pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += t;
+                }
+                nB = __shfl_sync(0xffffffffu, v, 31);
+                const int excl = v - h0 - h1;
+                __syncwarp();
+                hist[2 * lane] = excl;
+                hist[2 * lane + 1] = excl + h0;
+                __syncwarp();
             }
-            nB = __shfl_sync(0xffffffffu, v, 31);
-            const int excl = v - h0 - h1;
-            __syncwarp();
-            hist[2 * lane] = excl;
-            hist[2 * lane + 1] = excl + h0;
-            __syncwarp();
-        }
-        for (int base = 0; base < B; base += 32) {
-            const int b = base + lane;
-            const int r = b < B ? tail_of(lens[b]) : -1;
-            const int bucket = r >= 0 ? bucket_of(r) : kOrderBuckets;
-            const unsigned peers = same_key_lanes((unsigned)bucket);
-            if (bucket < kOrderBuckets) {
-                const unsigned below = peers & ((1u << lane) - 1u);
-                order[hist[bucket] + __popc(below)] = (uint16_t)b;
+            for (int base = 0; base < B; base += 32) {
+                const int b = base + lane;
+                const int r = b < B ? tail_of(lens[b]) : -1;
+                const int bucket = r >= 0 ? bucket_of(r) : kOrderBuckets;
+                const unsigned peers = same_key_lanes((unsigned)bucket);
+                if (bucket < kOrderBuckets) {
+                    const unsigned below = peers & ((1u << lane) - 1u);
+                    order[hist[bucket] + __popc(below)] = (uint16_t)b;
+                }
+                __syncwarp();
+                if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
+                __syncwarp();
             }
-            __syncwarp();
-            if (bucket < kOrderBuckets && lane == __ffs(peers) - 1) hist[bucket] += __popc(peers);
-            __syncwarp();
+            totalA = runningA;
         }
-        const int totalA = runningA;
         const int total = totalA + nB * HG;
 
         // Item -> (b, split, kvh) and its token range.

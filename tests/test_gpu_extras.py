@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 _CODE = {torch.float16: orc.F16, torch.bfloat16: orc.BF16, torch.float8_e4m3fn: orc.E4M3}
 
 
-def _run(kv, q, ps, cache_lens, batch_idx, leftpad, Hq=16, Hkv=2, D=128, num_splits=0, fuse=1, seed=0):
+def _run(kv, q, ps, cache_lens, batch_idx, leftpad, Hq=16, Hkv=2, D=128, num_splits=0, fuse=1, seed=0,
+         expect_flag=0):
     Bc = len(cache_lens)
     spec = W.Spec("ex", B=Bc, Hq=Hq, Hkv=Hkv, D=D, page_size=ps, kv=kv, q=q, lens=("list", cache_lens))
     wl = W.make(spec, 50 + seed, "cpu")
@@ -33,7 +34,7 @@ def _run(kv, q, ps, cache_lens, batch_idx, leftpad, Hq=16, Hkv=2, D=128, num_spl
             else:
                 wl.k_pages[page, slot] = float("nan")
                 wl.v_pages[page, slot] = float("nan")
-    attended = [int(cache_lens[r] - lp[r]) for r in rows]
+    attended = [int(cache_lens[r] - lp[r]) if 0 <= r < Bc else 0 for r in rows]
     prob = _lib.make_problem(Bq, Hq, Hkv, D, ps, wl.max_blocks, wl.num_pages, wl.q.dtype, wl.k_pages.dtype)
     plan = _lib.fd_plan(prob, attended, num_splits=num_splits, fuse_merge=fuse)
     g = wl.to("cuda")
@@ -47,6 +48,9 @@ def _run(kv, q, ps, cache_lens, batch_idx, leftpad, Hq=16, Hkv=2, D=128, num_spl
                             out, lse, ws, cache_batch_idx=bi, cache_leftpad=lpd,
                             cache_rows=Bc if batch_idx is not None else 0, status=status)
     torch.cuda.synchronize()
+    if expect_flag:
+        assert int(status.item()) & expect_flag
+        return
     assert int(status.item()) == 0
     p = orc.problem(Bq, Hq, Hkv, D, ps, wl.max_blocks, wl.num_pages, _CODE[wl.q.dtype], _CODE[wl.k_pages.dtype])
     ro, rl = orc.decode_paged_ex(p, Bc, None if batch_idx is None else np.asarray(batch_idx, np.int32),
@@ -74,3 +78,27 @@ def test_fp8_batch_index_and_leftpad(fdlib):
 
 def test_f16_leftpad_small_pages(fdlib):
     _run("f16", "f16", 16, [250, 64], None, [249, 1], Hq=8, Hkv=8, D=64, num_splits=4)
+
+
+def _large_batch_case(seed):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, 600, 200)
+    bi = rng.integers(0, 200, 300)
+    lp = np.array([int(rng.integers(0, n)) for n in lens])
+    return lens.tolist(), bi.tolist(), lp.tolist()
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+def test_large_batch_index_and_leftpad(fdlib, splits):
+    """300 q rows over 200 cache rows (permuted, with repeats) and left
+    padding: a batch of this size has its dispatch tables built by every warp
+    of the CTA, so cache-row indexing and padding go through that path."""
+    lens, bi, lp = _large_batch_case(11)
+    _run("bf16", "bf16", 16, lens, bi, lp, num_splits=splits)
+
+
+def test_large_batch_bad_index_is_flagged(fdlib):
+    """An index outside the cache in a large batch is flagged (not faulted)."""
+    lens, bi, lp = _large_batch_case(12)
+    bi[150] = len(lens)
+    _run("bf16", "bf16", 16, lens, bi, lp, num_splits=2, expect_flag=_lib.FD_DEV_BAD_PAGE)
