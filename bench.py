@@ -542,6 +542,38 @@ def bench_ex(args):
         "gpu_launches_per_call": 1}))
 
 
+def bench_large(args):
+    """The plain decode on two large batches (1024 bf16 sequences of 256-1024
+    tokens; 2048 FP8 sequences of 16-4096 tokens), timed back to back like the
+    headline; the dispatch tables of such batches are built by every warp."""
+    from split_kv_decode_paged_gb300 import workloads as W
+    from split_kv_decode_paged_gb300 import build as fd_build
+    fd_build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peak, kind = measured_peak()
+    cases = {}
+    for name, spec in W.LARGE_BATCHES.items():
+        wl = W.make(spec, W.LARGE_BATCH_SEED, dev)
+        ms, dec = time_decode(wl, args.steps, args.warmup, None)
+        us = statistics.mean(ms) * 1e3
+        nbytes = W.algorithmic_bytes(spec, wl.seq_lens.cpu())
+        cases[name] = {"workload": f"{spec.name}: B={spec.B}, Hq={spec.Hq}, Hkv={spec.Hkv}, D={spec.D}, {spec.kv}, "
+                                   f"{spec.page_size}-token pages, lengths {spec.lens} (seed {W.LARGE_BATCH_SEED})",
+                       "us_per_call": us, "bytes": nbytes, "gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak,
+                       "plan": {"num_splits": dec.plan.num_splits, "chunk_tokens": dec.plan.chunk_tokens,
+                                "stages": dec.plan.stages, "tile_tokens": dec.plan.tile_tokens}}
+        del wl, dec
+        torch.cuda.empty_cache()
+    head = cases["bf16 B=1024"]
+    print(json.dumps({
+        "metric": "decode-attention achieved HBM GB/s (large batches)", "value": head["gbs"], "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "us_per_call": head["us_per_call"],
+        "higher_is_better": True, "dtype": "bf16 / e4m3", "data": "synthetic", "cases": cases, "peak": peak,
+        "peak_source": kind, "config": {"workload": "large batches (value: the bf16 B=1024 case)",
+                                        "l2": "inputs > 2x L2: back to back, one event pair"},
+        "gpu_launches_per_call": 1}))
+
+
 def bench_merge(args):
     """fd_merge_states on fp32 partial states [B=64, Hq=32, S=8, D=128] to a
     bf16 output, L2 flushed before every call."""
@@ -586,7 +618,7 @@ def main():
     ap.add_argument("--all-configs", action="store_true", help="also report every workload (per_config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge", "ex"],
+    ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge", "ex", "large"],
                     help="cascade: shared-prefix batch, cascade vs plain decode; append: fd_append_kv (plain "
                          "and rotary); merge: fd_merge_states; ex: fd_decode_paged_ex with cache_batch_idx "
                          "and left padding")
@@ -600,7 +632,8 @@ def main():
             print(json.dumps({"impl": "reference",
                               "unavailable": f"the {args.workload} workload is measured on the GPU path only"}))
             return
-        {"cascade": bench_cascade, "append": bench_append, "merge": bench_merge, "ex": bench_ex}[args.workload](args)
+        {"cascade": bench_cascade, "append": bench_append, "merge": bench_merge, "ex": bench_ex,
+         "large": bench_large}[args.workload](args)
         return
     from split_kv_decode_paged_gb300 import workloads as W
     ws, rank, local = dist_env()

@@ -12,6 +12,8 @@
 // for GQA).  Sequences shorter than one chunk are not split.  Items are
 // dispatched longest first -- every full chunk, then each sequence's partial
 // chunk sorted by length -- through an atomic counter to a persistent grid.
+// Every CTA builds the same order in shared memory from seq_lens at start:
+// the producer alone for small batches, all warps for large ones.
 //
 // CTA layout: NC consumer warps + 1 producer warp.
 //   producer: claims items one ahead, reads the block table a batch of 32
@@ -22,8 +24,9 @@
 //   consumers: each warp takes SUBT sub-tiles of 16 tokens of every stage:
 //     S^T[16 tok x 8 heads] = K[16 x D] . Q^T  (mma.sync m16n8k16, K from
 //     swizzled shared memory via ldmatrix, Q in registers),
-//     online softmax in the exp2 domain (the reference maximum moves only when
-//     a score passes it by more than kMaxSlack), P^T moved into the B operand
+//     one online-softmax step over the warp's sub-tiles in the exp2 domain
+//     (the reference maximum moves only when a score passes it by more than
+//     kMaxSlack), P^T moved into the B operand
 //     with movmatrix, O^T[D x 8] += V^T[D x 16] . P^T (ldmatrix.trans on V).
 //     At the end of an item the warps merge their states (warp w+NC/2 into
 //     warp w, then through shared memory); a single-split item writes
@@ -677,13 +680,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const int b = cur.b, s = cur.s, kvh = cur.kvh, nsplit = cur.nsplit;
             const int t_begin = cur.t_begin, t_end = cur.t_end, ntok = cur.ntok, ntiles = cur.ntiles;
             const int nbox = cur.nbox, box0 = cur.box0;
-            float ks_cur = 1.f, vs_cur = 1.f;
-            if constexpr (FP8) {
-                if (pg_cur >= 0 && pg_cur < p.num_pages) {
-                    ks_cur = __ldg(p.k_scale + (size_t)pg_cur * Hkv + kvh);
-                    vs_cur = __ldg(p.v_scale + (size_t)pg_cur * Hkv + kvh);
-                }
-            }
             int batch = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int kb = j * BPT;
@@ -691,20 +687,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     ++batch;
                     pg_cur = pg_nxt;
                     pg_nxt = page_of(cur, (batch + 1) * 32 + lane);
-                    if constexpr (FP8) {
-                        if (pg_cur >= 0 && pg_cur < p.num_pages) {
-                            ks_cur = __ldg(p.k_scale + (size_t)pg_cur * Hkv + kvh);
-                            vs_cur = __ldg(p.v_scale + (size_t)pg_cur * Hkv + kvh);
-                        }
-                    }
                 }
                 const int src_lane = (kb + (lane < BPT ? lane : 0)) & 31;
                 const int pg = __shfl_sync(0xffffffffu, pg_cur, src_lane);
-                float ksc = 1.f, vsc = 1.f;
-                if constexpr (FP8) {
-                    ksc = __shfl_sync(0xffffffffu, ks_cur, src_lane);
-                    vsc = __shfl_sync(0xffffffffu, vs_cur, src_lane);
-                }
                 const bool live = lane < BPT && (kb + lane) < nbox;
                 const bool good = live && pg >= 0 && pg < p.num_pages;
                 if (live && !good) flag_status(p.status, FD_DEV_BAD_PAGE);
@@ -729,14 +714,21 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     m->flags = (j == 0 ? kFlagFirst : 0) | (j == ntiles - 1 ? kFlagLast : 0);
                     m->nsplit = nsplit;
                 }
+                const uint32_t fb = smem_u32(&full_bar[st]);
                 if constexpr (FP8) {
-                    if (lane < BPT) {
-                        m->kscale[lane] = ksc;
-                        m->vscale[lane] = vsc;
+                    // Per-(page, KV head) scales of the tile's boxes, copied
+                    // asynchronously; the stage's full barrier also waits for
+                    // them (registered before lane 0's arrival below).
+                    if (good) {
+                        cp_async_4(smem_u32(&m->kscale[lane]), p.k_scale + (size_t)pg * Hkv + kvh);
+                        cp_async_4(smem_u32(&m->vscale[lane]), p.v_scale + (size_t)pg * Hkv + kvh);
+                        cp_async_mbar_arrive(fb);
+                    } else if (lane < BPT) {
+                        m->kscale[lane] = 1.f;
+                        m->vscale[lane] = 1.f;
                     }
                 }
                 __syncwarp();
-                const uint32_t fb = smem_u32(&full_bar[st]);
                 if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
                 __syncwarp();
                 uint8_t *sb = stages + (size_t)st * Sh::STAGE;

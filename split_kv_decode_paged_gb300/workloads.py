@@ -63,6 +63,17 @@ CONFIGS = {
 }
 
 
+# Two large batches beyond the five workloads (many 32-row blocks of the
+# dispatch tables): short bf16 contexts, and an FP8 cache with a wide length mix.
+LARGE_BATCHES = {
+    "bf16 B=1024": Spec("large GQA batch, short contexts", B=1024, Hq=32, Hkv=8, D=128, page_size=16, kv="bf16",
+                        q="bf16", lens=("uniform", 256, 1024), pool=("factor", 1.1)),
+    "e4m3 B=2048": Spec("large FP8 batch, mixed lengths", B=2048, Hq=32, Hkv=8, D=128, page_size=64, kv="e4m3",
+                        q="bf16", lens=("loguniform", 16, 4096), pool=("factor", 1.1)),
+}
+LARGE_BATCH_SEED = 77
+
+
 def config_seed(cfg_id: int) -> int:
     return 1000 + int(cfg_id)
 
