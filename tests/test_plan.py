@@ -106,6 +106,10 @@ def test_head_subgroups_and_shared_kv(fdlib):
     (torch.float8_e4m3fn, 128, 256, 128, 128, None),  # explicit request
     (torch.bfloat16, 128, 256, 256, 128, 3),       # 256-token stages are E4M3 only
     (torch.bfloat16, 16, 1024, 0, 128, 3),
+    (torch.bfloat16, 16, 1712, 0, 128, 3),         # the dispatch tables (~6 B per sequence) set
+    (torch.bfloat16, 16, 1728, 0, 128, 2),         # where 3 stages stop fitting ...
+    (torch.float8_e4m3fn, 128, 1712, 0, 256, 3),   # ... and where 256-token E4M3 stages do
+    (torch.float8_e4m3fn, 128, 1728, 0, 128, None),
     (torch.bfloat16, 16, 8192, 0, 128, 2),         # the largest batch still plans
 ])
 def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
