@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
     FD_OK = 0,
     FD_ERR_INVALID_ARG = 1,         /* null pointer, bad size, bad alignment          */
-    FD_ERR_UNSUPPORTED = 2,         /* a valid problem this build does not serve      */
+    FD_ERR_UNSUPPORTED = 2,         /* a valid problem this library does not serve    */
     FD_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < plan->workspace_bytes        */
     FD_ERR_BAD_PAGE = 4,            /* device saw a block-table entry out of range    */
     FD_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed              */
