@@ -68,7 +68,10 @@ class PagedDecoder:
                                   io.host_out, self.workspace, self.status, stream)
 
     def check(self):
-        """Synchronise and raise FdError if the device reported an error."""
+        """Synchronise the decoder's device (calls may run on any stream) and
+        raise FdError if the device reported an error."""
+        if self.device.type == "cuda":
+            torch.cuda.synchronize(self.device)
         word = int(self.status.item())
         if word:
             self.status.zero_()
