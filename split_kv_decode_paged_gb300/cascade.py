@@ -55,6 +55,9 @@ class CascadeDecoder:
         return out, lse
 
     def check(self):
+        """Synchronise the device and raise FdError if a kernel reported an error."""
+        if self.device.type == "cuda":
+            torch.cuda.synchronize(self.device)
         word = int(self.status.item())
         if word:
             self.status.zero_()
