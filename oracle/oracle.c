@@ -8,12 +8,13 @@
  *
  * Passages followed (page title, section):
  *  - "FlashDecoding 与 FlashInfer 深度解析", §2.1 step 2 (score = q k^T / sqrt(d),
- *    softmax, weighted sum of V, local max and sum) and the merge code block of
- *    step 3 (global max, rescale factors exp(max_i - global max), weighted sums).
+ *    softmax, weighted sum of V, local max and sum).
  *  - lpnh.cn "FlashDecoding 核心原理", stage one (partial state: unnormalised
- *    output, local max m_i, denominator d_i) and stage two (m_global = max m_i,
- *    alpha_i = exp(m_i - m_global), d_global = sum alpha_i d_i,
- *    O = sum alpha_i O_i / d_global).
+ *    output, local max m_i, denominator d_i) and the stage-two formula
+ *    (m_global = max m_i, alpha_i = exp(m_i - m_global), d_global =
+ *    sum alpha_i d_i, O = sum alpha_i O_i / d_global), evaluated here through
+ *    its log-sum-exp: lse = m_global + ln d_global, and the weight of piece i
+ *    alpha_i / d_global = exp(m_i - lse).
  *  - "Inference Cookbook" (FlashAttention), §4.2: paged pools
  *    [num_pages, page_size, Hkv, D] and a block table whose unused entries
  *    are -1; §3.5: softmax_lse per (batch, head); §7: FP8 KV with per-head
@@ -379,27 +380,30 @@ int orc_partial_state(const orc_problem *p, const void *q, const void *k_pages,
     return partial(&in, b, hq, t_begin, t_end, o, m, d);
 }
 
-/* Stage two of the pages: m_g = max_i m_i; alpha_i = exp(m_i - m_g);
- * d_g = sum alpha_i d_i; out = sum alpha_i o_i / d_g; lse = m_g + ln d_g.
- * Empty partials (m = -inf) get alpha = 0; all-empty gives out = 0,
- * lse = -inf. */
+/* Stage two of lpnh.cn "FlashDecoding 核心原理": the merged log-sum-exp is
+ * lse = m_g + ln(sum_i exp(m_i - m_g) d_i) with m_g = max_i m_i; each piece
+ * then enters the output with the weight exp(m_i - lse) (its alpha_i divided
+ * by the merged denominator), out = sum_i exp(m_i - lse) o_i.  Empty pieces
+ * (m = -inf) have weight 0; all empty gives out = 0, lse = -inf. */
 void orc_merge_states(int n, int D, const double *o, const double *m, const double *d,
                       double *out, double *lse) {
+    for (int k = 0; k < D; ++k) out[k] = 0.0;
     double mg = -INFINITY;
     for (int i = 0; i < n; ++i) if (m[i] > mg) mg = m[i];
-    for (int k = 0; k < D; ++k) out[k] = 0.0;
     if (mg == -INFINITY) {
         *lse = -INFINITY;
         return;
     }
-    double dg = 0.0;
+    double z = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (m[i] != -INFINITY) z += exp(m[i] - mg) * d[i];
+    const double l = mg + log(z);
     for (int i = 0; i < n; ++i) {
-        double alpha = (m[i] == -INFINITY) ? 0.0 : exp(m[i] - mg);
-        dg += alpha * d[i];
-        for (int k = 0; k < D; ++k) out[k] += alpha * o[(size_t)i * D + k];
+        if (m[i] == -INFINITY) continue;
+        const double w = exp(m[i] - l);
+        for (int k = 0; k < D; ++k) out[k] += w * o[(size_t)i * D + k];
     }
-    for (int k = 0; k < D; ++k) out[k] /= dg;
-    *lse = mg + log(dg);
+    *lse = l;
 }
 
 int orc_append_kv(const orc_problem *p, int new_dtype, const void *k_new, const void *v_new,
