@@ -1,7 +1,9 @@
 """GPU parity tests: the CUDA decode path (through the C ABI) against the fp64
 oracle on the same seeded inputs, plus bit-exact paging and device-error
 reporting.  Bars: out max-abs <= 2e-3 and lse <= 1e-3 for f16/bf16 K/V,
-out <= 3e-2 for E4M3 K/V (oracle on the dequantised stored values)."""
+out <= 3e-2 for E4M3 K/V (oracle on the dequantised stored values), plus half
+an output ulp when the output is f16/bf16.  The five benchmark workloads are
+checked row by row in test_gpu_configs.py."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +11,7 @@ import torch
 import split_kv_decode_paged_gb300 as fd
 from split_kv_decode_paged_gb300 import _lib
 from split_kv_decode_paged_gb300 import workloads as W
-from tests.gpu_helpers import (TOL_OUT, assert_close, gpu_decode, oracle_full, oracle_pairs)
+from tests.gpu_helpers import assert_close, gpu_decode, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -69,45 +71,6 @@ def test_small_shapes(fdlib, case, splits, out32):
 def test_fp32_output(fdlib, kv, q):
     spec = _spec("f32 out", 2, 8, 2, 128, 16, kv, q, [90, 333])
     _run_and_check(spec, seed=3, out_dtype=torch.float32, num_splits=2)
-
-
-def test_config2_single_sequence_mha(fdlib):
-    wl = W.make_config(2, "cpu")
-    out, lse, dec = gpu_decode(wl.to("cuda"))
-    assert dec.plan.num_splits > 1
-    ref_o, ref_l = oracle_full(wl)
-    assert_close("f16", out, lse, ref_o, ref_l, "cfg2")
-
-
-def test_config4_long_context(fdlib):
-    wl = W.make_config(4, "cpu")
-    out, lse, dec = gpu_decode(wl.to("cuda"))
-    assert 16 <= dec.plan.num_splits <= 64
-    ref_o, ref_l = oracle_full(wl)
-    assert_close("bf16", out, lse, ref_o, ref_l, "cfg4")
-
-
-def _sample_pairs(wl, n, seed):
-    lens = wl.seq_lens.cpu().numpy()
-    B, Hq = wl.spec.B, wl.spec.Hq
-    rng = np.random.default_rng(seed)
-    bs = [int(np.argmax(lens)), int(np.argmin(lens)), 0, B - 1] + rng.integers(0, B, n).tolist()
-    return [(b, int(rng.integers(0, Hq))) for b in bs] + [(int(np.argmax(lens)), Hq - 1)]
-
-
-@pytest.mark.parametrize("cfg", [3, 5])
-def test_batched_configs_sampled(fdlib, cfg):
-    wl = W.make_config(cfg, "cuda")
-    out, lse, dec = gpu_decode(wl)
-    wl_cpu = wl.to("cpu")
-    pairs = _sample_pairs(wl_cpu, 40, cfg)
-    ref_o, ref_l = oracle_pairs(wl_cpu, pairs)
-    idx_b = torch.tensor([p[0] for p in pairs])
-    idx_h = torch.tensor([p[1] for p in pairs])
-    o = out.cpu()[idx_b, idx_h]
-    l = lse.cpu()[idx_b, idx_h]
-    assert_close(wl.spec.kv, o, l, ref_o, ref_l, f"cfg{cfg} sampled")
-    assert torch.isfinite(out.float()).all()
 
 
 def test_paged_equals_contiguous_bitexact(fdlib):

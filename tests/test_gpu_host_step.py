@@ -8,7 +8,7 @@ import torch
 import split_kv_decode_paged_gb300 as fd
 from oracle import oracle as orc
 from split_kv_decode_paged_gb300 import workloads as W
-from tests.gpu_helpers import assert_close
+from tests.gpu_helpers import assert_close, record_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -21,11 +21,13 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("out32", [False, True], ids=["out-native", "out-f32"])
 @pytest.mark.parametrize("spec", CASES, ids=[c.name for c in CASES])
-def test_host_step_matches_device_call_and_oracle(fdlib, spec):
+def test_host_step_matches_device_call_and_oracle(fdlib, spec, out32):
     wl = W.make(spec, 31, "cpu")
     g = wl.to("cuda")
-    dec = fd.PagedDecoder.for_pools(g.q, g.k_pages, g.v_pages, g.block_table, wl.seq_lens)
+    dec = fd.PagedDecoder.for_pools(g.q, g.k_pages, g.v_pages, g.block_table, wl.seq_lens,
+                                    out_dtype=torch.float32 if out32 else None)
     ref_out, ref_lse = dec(g.q, g.k_pages, g.v_pages, g.block_table, g.seq_lens, g.k_scale, g.v_scale)
     torch.cuda.synchronize()
     dec.check()
@@ -45,7 +47,9 @@ def test_host_step_matches_device_call_and_oracle(fdlib, spec):
                     _CODE[wl.q.dtype], _CODE[wl.k_pages.dtype])
     ro, rl = orc.decode_paged(p, wl.q, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale, wl.block_table,
                               wl.seq_lens)
-    assert_close(spec.kv, io.out, io.lse, ro, rl, f"host step {spec.name}")
+    err_o, err_l = assert_close(spec.kv, io.out, io.lse, ro, rl, f"host step {spec.name}")
+    record_errors(f"host step {spec.name}", out_dtype=str(io.out.dtype).replace("torch.", ""),
+                  out_max_abs_err=err_o, lse_max_abs_err=err_l)
 
 
 def test_host_step_pageable_output_block_is_copied(fdlib):
