@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define FD_API_VERSION 1
+#define FD_API_VERSION 2
 
 typedef enum {
     FD_OK = 0,
@@ -109,6 +109,17 @@ typedef struct {
                            the B*G q rows of each KV head are packed 16 to a
                            work item so each K/V tile feeds 16 rows; plan with
                            seq_lens_host[0] = the shared length */
+    int timeout_us;     /* limit of every device-side wait, in microseconds;
+                           0 = 2 s.  A wait that runs past it sets
+                           FD_DEV_TIMEOUT, and the kernel drains its copies in
+                           flight and returns (no trap, no hang)  */
+    int debug_stall_us; /* TEST HOOK, 0 = off: with debug_stall_role 1 the
+                           producer warp of every CTA idles this long before
+                           its first load; with 2 the consumer warps idle this
+                           long before releasing their first stage.  Longer
+                           than timeout_us, it makes the other side's waits
+                           run out, exercising the timeout path.  <= 1 s.   */
+    int debug_stall_role; /* 0, 1 (producer) or 2 (consumers)                */
 } fd_plan_options;
 
 /* A plan: plain data in host memory, owned by the caller, reusable for any
@@ -132,7 +143,10 @@ typedef struct {
     int kv_rows;          /* block-table / seq_lens rows the call reads          */
     int row_fold;         /* q sequences per KV row (1, or B with shared_kv)     */
     int head_subgroups;   /* work items per (KV row, split, KV head)             */
-    int reserved[5];
+    int timeout_us;       /* device wait limit (0 = 2 s), from the options       */
+    int debug_stall_us;   /* test hook copied from the options (0 = off)         */
+    int debug_stall_role;
+    int reserved[2];
 } fd_plan_t;
 
 /* Plan a decode call [P1 §2.1 step 1; P2 进阶突破; P3 §6.3, §8.2].

@@ -76,6 +76,10 @@ class PagedDecoder:
         if word:
             self.status.zero_()
             self.workspace.zero_()
+            if self.device.type == "cuda":
+                # the clears are queued on the current stream: finish them
+                # before a call on any other stream can touch the workspace
+                torch.cuda.synchronize(self.device)
             raise FdError(fd_status_from_device(word), "device status")
 
 

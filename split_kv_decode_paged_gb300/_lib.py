@@ -48,7 +48,8 @@ class FdProblem(ctypes.Structure):
 class FdPlanOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("num_sms", ctypes.c_int), ("fuse_merge", ctypes.c_int),
                 ("max_seq_len", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("split_margin_pct", ctypes.c_int),
-                ("tile_tokens", ctypes.c_int), ("shared_kv", ctypes.c_int)]
+                ("tile_tokens", ctypes.c_int), ("shared_kv", ctypes.c_int), ("timeout_us", ctypes.c_int),
+                ("debug_stall_us", ctypes.c_int), ("debug_stall_role", ctypes.c_int)]
 
 
 class FdDecodeExtras(ctypes.Structure):
@@ -64,7 +65,8 @@ class FdPlan(ctypes.Structure):
                 ("ws_partial_o", ctypes.c_size_t), ("ws_partial_md", ctypes.c_size_t),
                 ("ws_counters", ctypes.c_size_t), ("work_items_hint", ctypes.c_longlong),
                 ("kv_rows", ctypes.c_int), ("row_fold", ctypes.c_int), ("head_subgroups", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+                ("timeout_us", ctypes.c_int), ("debug_stall_us", ctypes.c_int), ("debug_stall_role", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n not in ("problem", "reserved")}
@@ -131,6 +133,82 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+class _Args:
+    """Checks of the tensors handed to one entry point against the shapes and
+    dtypes the C ABI expects (the ABI sees only pointers).  Every failure
+    raises ValueError before anything is launched.  Shapes, dtypes and
+    layout are checked as each tensor is named; placement last (done()):
+    device tensors must all sit on one CUDA device, host blocks on the CPU."""
+
+    def __init__(self, entry):
+        self.entry = entry
+        self.placed = []
+
+    def _fail(self, name, what):
+        raise ValueError(f"{self.entry}: {name} {what}")
+
+    def tensor(self, name, t, dtype=None, shape=None, min_bytes=None, host=False, optional=False):
+        if t is None:
+            if optional:
+                return
+            self._fail(name, "is required")
+        if not isinstance(t, torch.Tensor):
+            self._fail(name, f"must be a torch.Tensor, got {type(t).__name__}")
+        if dtype is not None and t.dtype != dtype:
+            self._fail(name, f"must have dtype {dtype}, got {t.dtype}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            self._fail(name, f"must have shape {tuple(shape)}, got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            self._fail(name, "must be contiguous")
+        if min_bytes is not None and t.numel() * t.element_size() < min_bytes:
+            self._fail(name, f"must hold at least {min_bytes} bytes, got {t.numel() * t.element_size()}")
+        self.placed.append((name, t, host))
+
+    def absent(self, name, t, why):
+        if t is not None:
+            self._fail(name, f"must be None ({why})")
+
+    def done(self):
+        device = None
+        for name, t, host in self.placed:
+            if host:
+                if t.device.type != "cpu":
+                    self._fail(name, f"must be a host (CPU) tensor, got {t.device}")
+                continue
+            if t.device.type != "cuda":
+                self._fail(name, f"must be a CUDA tensor, got {t.device}")
+            if device is None:
+                device = t.device
+            elif t.device != device:
+                self._fail(name, f"is on {t.device}, other arguments on {device}")
+
+
+def _check_decode(entry, plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse, workspace,
+                  status, table_rows=None, host_io=False):
+    p = plan.problem
+    a = _Args(entry)
+    kv = FD_TO_TORCH[p.kv_dtype]
+    pool = (p.num_pages, p.page_size, p.Hkv, p.D)
+    rows = table_rows if table_rows is not None else (plan.kv_rows if plan.kv_rows > 0 else p.B)
+    if not host_io:
+        a.tensor("q", q, FD_TO_TORCH[p.q_dtype], (p.B, p.Hq, p.D))
+        a.tensor("block_table", block_table, torch.int32, (rows, p.max_blocks_per_seq))
+        a.tensor("seq_lens", seq_lens, torch.int32, (rows,))
+        a.tensor("out", out, FD_TO_TORCH[p.out_dtype], (p.B, p.Hq, p.D))
+        a.tensor("lse", lse, torch.float32, (p.B, p.Hq), optional=True)
+    a.tensor("k_pages", k_pages, kv, pool)
+    a.tensor("v_pages", v_pages, kv, pool)
+    if p.kv_dtype == FD_E4M3:
+        a.tensor("k_scale", k_scale, torch.float32, (p.num_pages, p.Hkv))
+        a.tensor("v_scale", v_scale, torch.float32, (p.num_pages, p.Hkv))
+    else:
+        a.absent("k_scale", k_scale, "the cache is not E4M3")
+        a.absent("v_scale", v_scale, "the cache is not E4M3")
+    a.tensor("workspace", workspace, None, None, min_bytes=int(plan.workspace_bytes))
+    a.tensor("status", status, torch.int32, None, min_bytes=4, optional=True)
+    return a
+
+
 def fd_status_string(code: int) -> str:
     return load().fd_status_string(int(code)).decode()
 
@@ -150,13 +228,17 @@ def make_problem(B, Hq, Hkv, D, page_size, max_blocks_per_seq, num_pages, q_dtyp
 
 
 def fd_plan(problem: FdProblem, seq_lens_host, num_splits=0, num_sms=0, fuse_merge=1, max_seq_len=0,
-            ctas_per_sm=0, split_margin_pct=0, tile_tokens=0, shared_kv=0) -> FdPlan:
-    """Plan a decode call; seq_lens_host is a host int32 tensor/sequence."""
+            ctas_per_sm=0, split_margin_pct=0, tile_tokens=0, shared_kv=0, timeout_us=0, debug_stall_us=0,
+            debug_stall_role=0) -> FdPlan:
+    """Plan a decode call; seq_lens_host is a host int32 tensor/sequence.
+    timeout_us bounds every device-side wait (0 = 2 s); debug_stall_us and
+    debug_stall_role are the test hook of the timeout path (0 = off)."""
     lens = torch.as_tensor(seq_lens_host, dtype=torch.int32).cpu().contiguous()
     if lens.numel() != problem.B and not (shared_kv and lens.numel() >= 1):
         raise ValueError("seq_lens_host must have B entries")
     opts = FdPlanOptions(int(num_splits), int(num_sms), int(fuse_merge), int(max_seq_len), int(ctas_per_sm),
-                         int(split_margin_pct), int(tile_tokens), int(shared_kv))
+                         int(split_margin_pct), int(tile_tokens), int(shared_kv), int(timeout_us),
+                         int(debug_stall_us), int(debug_stall_role))
     plan = FdPlan()
     rc = load().fd_plan(ctypes.byref(problem), ctypes.c_void_p(lens.data_ptr()), ctypes.byref(opts),
                         ctypes.byref(plan))
@@ -167,6 +249,8 @@ def fd_plan(problem: FdProblem, seq_lens_host, num_splits=0, num_sms=0, fuse_mer
 
 def fd_decode_paged(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
                     workspace, status=None, stream=None):
+    _check_decode("fd_decode_paged", plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
+                  workspace, status).done()
     rc = load().fd_decode_paged(ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                 _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse),
                                 _ptr(workspace), int(workspace.numel() * workspace.element_size()),
@@ -177,6 +261,13 @@ def fd_decode_paged(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, block_t
 
 def fd_decode_paged_ex(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
                        workspace, cache_batch_idx=None, cache_leftpad=None, cache_rows=0, status=None, stream=None):
+    p = plan.problem
+    rows = int(cache_rows) if cache_batch_idx is not None else (plan.kv_rows if plan.kv_rows > 0 else p.B)
+    a = _check_decode("fd_decode_paged_ex", plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out,
+                      lse, workspace, status, table_rows=rows)
+    a.tensor("cache_batch_idx", cache_batch_idx, torch.int32, (p.B,), optional=True)
+    a.tensor("cache_leftpad", cache_leftpad, torch.int32, (rows,), optional=True)
+    a.done()
     ex = FdDecodeExtras(None if cache_batch_idx is None else cache_batch_idx.data_ptr(),
                         None if cache_leftpad is None else cache_leftpad.data_ptr(), int(cache_rows))
     rc = load().fd_decode_paged_ex(ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
@@ -189,15 +280,49 @@ def fd_decode_paged_ex(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, bloc
 
 def fd_merge_states(o_part, m, d, out, lse=None, stream=None):
     """o_part [B,Hq,S,D] fp32, m/d [B,Hq,S] fp32 -> out [B,Hq,D], lse [B,Hq]."""
+    a = _Args("fd_merge_states")
+    a.tensor("o_part", o_part, torch.float32)
+    if o_part.dim() != 4:
+        a._fail("o_part", f"must be 4-D [B, Hq, S, D], got shape {tuple(o_part.shape)}")
     B, Hq, S, D = o_part.shape
+    a.tensor("m", m, torch.float32, (B, Hq, S))
+    a.tensor("d", d, torch.float32, (B, Hq, S))
+    if out is None or out.dtype not in (torch.float16, torch.bfloat16, torch.float32):
+        a._fail("out", "must be a float16, bfloat16 or float32 tensor")
+    a.tensor("out", out, None, (B, Hq, D))
+    a.tensor("lse", lse, torch.float32, (B, Hq), optional=True)
+    a.done()
     rc = load().fd_merge_states(_ptr(o_part), _ptr(m), _ptr(d), B, Hq, S, D, fd_dtype(out.dtype), _ptr(out),
                                 _ptr(lse), _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_merge_states")
 
 
+def _check_append(entry, p, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, status):
+    a = _Args(entry)
+    kv = FD_TO_TORCH[p.kv_dtype]
+    new = FD_TO_TORCH[p.q_dtype] if p.kv_dtype == FD_E4M3 else kv
+    a.tensor("k_new", k_new, new, (p.B, p.Hkv, p.D))
+    a.tensor("v_new", v_new, new, (p.B, p.Hkv, p.D))
+    pool = (p.num_pages, p.page_size, p.Hkv, p.D)
+    a.tensor("k_pages", k_pages, kv, pool)
+    a.tensor("v_pages", v_pages, kv, pool)
+    if p.kv_dtype == FD_E4M3:
+        a.tensor("k_scale", k_scale, torch.float32, (p.num_pages, p.Hkv))
+        a.tensor("v_scale", v_scale, torch.float32, (p.num_pages, p.Hkv))
+    else:
+        a.absent("k_scale", k_scale, "the cache is not E4M3")
+        a.absent("v_scale", v_scale, "the cache is not E4M3")
+    a.tensor("block_table", block_table, torch.int32, (p.B, p.max_blocks_per_seq))
+    a.tensor("seq_lens", seq_lens, torch.int32, (p.B,))
+    a.tensor("status", status, torch.int32, None, min_bytes=4, optional=True)
+    return a
+
+
 def fd_append_kv(problem: FdProblem, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens,
                  status=None, stream=None):
+    _check_append("fd_append_kv", problem, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens,
+                  status).done()
     rc = load().fd_append_kv(ctypes.byref(problem), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
                              _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(status),
                              _stream(stream))
@@ -209,6 +334,14 @@ def fd_append_kv_rotary(problem: FdProblem, k_new, v_new, k_pages, v_pages, k_sc
                         seq_lens, rotary_cos, rotary_sin, interleaved=False, q_inout=None, status=None,
                         stream=None):
     """rotary_cos/sin: fp32 [max_pos, rotary_dim/2] on the device."""
+    a = _check_append("fd_append_kv_rotary", problem, k_new, v_new, k_pages, v_pages, k_scale, v_scale, block_table,
+                      seq_lens, status)
+    a.tensor("rotary_cos", rotary_cos, torch.float32)
+    if rotary_cos.dim() != 2:
+        a._fail("rotary_cos", f"must be 2-D [max_pos, rotary_dim / 2], got shape {tuple(rotary_cos.shape)}")
+    a.tensor("rotary_sin", rotary_sin, torch.float32, tuple(rotary_cos.shape))
+    a.tensor("q_inout", q_inout, FD_TO_TORCH[problem.q_dtype], (problem.B, problem.Hq, problem.D), optional=True)
+    a.done()
     max_pos, half = rotary_cos.shape
     rc = load().fd_append_kv_rotary(ctypes.byref(problem), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
                                     _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
@@ -220,6 +353,18 @@ def fd_append_kv_rotary(problem: FdProblem, k_new, v_new, k_pages, v_pages, k_sc
 
 def fd_merge_two(out_a, lse_a, out_b, lse_b, out, lse=None, stream=None):
     """out_a/out_b fp32 [..., D], lse_a/lse_b fp32 [...] -> out [..., D], lse."""
+    a = _Args("fd_merge_two")
+    a.tensor("out_a", out_a, torch.float32)
+    if out_a.dim() < 1:
+        a._fail("out_a", "must have a last dimension D")
+    a.tensor("out_b", out_b, torch.float32, tuple(out_a.shape))
+    a.tensor("lse_a", lse_a, torch.float32, tuple(out_a.shape[:-1]))
+    a.tensor("lse_b", lse_b, torch.float32, tuple(out_a.shape[:-1]))
+    if out is None or out.dtype not in (torch.float16, torch.bfloat16, torch.float32):
+        a._fail("out", "must be a float16, bfloat16 or float32 tensor")
+    a.tensor("out", out, None, tuple(out_a.shape))
+    a.tensor("lse", lse, torch.float32, tuple(out_a.shape[:-1]), optional=True)
+    a.done()
     D = out_a.shape[-1]
     rows = out_a.numel() // D
     rc = load().fd_merge_two(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), rows, D, fd_dtype(out.dtype),
@@ -238,6 +383,14 @@ def fd_host_io_layout_for(plan: FdPlan) -> FdHostIoLayout:
 
 def fd_decode_paged_host(plan: FdPlan, host_in, dev_in, k_pages, v_pages, k_scale, v_scale, dev_out, host_out,
                          workspace, status=None, stream=None):
+    lay = fd_host_io_layout_for(plan)
+    a = _check_decode("fd_decode_paged_host", plan, None, k_pages, v_pages, k_scale, v_scale, None, None, None,
+                      None, workspace, status, host_io=True)
+    a.tensor("host_in", host_in, None, None, min_bytes=int(lay.in_bytes), host=True)
+    a.tensor("host_out", host_out, None, None, min_bytes=int(lay.out_bytes), host=True)
+    a.tensor("dev_in", dev_in, None, None, min_bytes=int(lay.in_bytes))
+    a.tensor("dev_out", dev_out, None, None, min_bytes=int(lay.out_bytes))
+    a.done()
     rc = load().fd_decode_paged_host(ctypes.byref(plan), _ptr(host_in), _ptr(dev_in), _ptr(k_pages), _ptr(v_pages),
                                      _ptr(k_scale), _ptr(v_scale), _ptr(dev_out), _ptr(host_out), _ptr(workspace),
                                      int(workspace.numel() * workspace.element_size()), _ptr(status),

@@ -63,4 +63,7 @@ class CascadeDecoder:
             self.status.zero_()
             self.ws_p.zero_()
             self.ws_s.zero_()
+            if self.device.type == "cuda":
+                # finish the clears before a call on another stream runs
+                torch.cuda.synchronize(self.device)
             raise _lib.FdError(_lib.fd_status_from_device(word), "device status")

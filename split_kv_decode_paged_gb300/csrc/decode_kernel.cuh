@@ -35,7 +35,9 @@
 //     of them (atomic counter, no spin-wait), per the merge formula of stage
 //     two.
 // FP8 (E4M3) K/V are converted to f16 in registers (exact); the per-(page,
-// KV head) scales multiply the scores and the P.V product.
+// KV head) scales multiply the scores and the P.V product.  A bf16 q enters
+// that f16 product scaled per head by a power of two (exact in f16 over the
+// head's whole range), undone on the scores.
 #pragma once
 
 #include <float.h>
@@ -106,6 +108,12 @@ __device__ __forceinline__ unsigned same_key_lanes(unsigned key) {
         m &= set ? v : ~v;
     }
     return m;
+}
+
+// Idle for ns nanoseconds (the stall test hook of the timeout path).
+__device__ __forceinline__ void idle_ns(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
 __device__ __forceinline__ void flag_status(int *status, int bit) {
@@ -672,6 +680,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             npg0 = page_of(nx, lane);
             npg1 = page_of(nx, 32 + lane);
         }
+        if (p.stall_role == 1) idle_ns(p.stall_ns);  // test hook: late producer
         while (ok && next_item < total) {
             const Item cur = nx;
             int pg_cur = npg0, pg_nxt = npg1;
@@ -770,14 +779,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // No more items to claim: the next grid in the stream may start
         // launching onto SMs as they free up.
         grid_launch_dependents();
-        if (!ok) {
-            // Abort: wait (bounded) for the copies still in flight into the
-            // stages issued most recently before leaving.
-            for (int k = 1; k <= NST && k <= n_issued; ++k) {
-                const int s2 = (st - k + NST) % NST;
-                const uint32_t par = (s2 < st) ? ph : (ph ^ 1u);
-                mbar_wait_bounded(smem_u32(&full_bar[s2]), par, p.timeout_ns);
-            }
+        // Wait (bounded) until the copies into the stages issued most recently
+        // have landed: the consumers leave early when one of their own waits
+        // runs out, and no copy may still be in flight when the CTA exits.
+        // Only this warp arrives on the full barriers, so the phase of each
+        // stage's last issue is still the one its parity names.
+        for (int k = 1; k <= NST && k <= n_issued; ++k) {
+            const int s2 = (st - k + NST) % NST;
+            const uint32_t par = (s2 < st) ? ph : (ph ^ 1u);
+            if (!mbar_wait_bounded(smem_u32(&full_bar[s2]), par, p.timeout_ns)) ok = false;
         }
         // Stop marker for the consumers.
         if (ok && mbar_wait_bounded(smem_u32(&empty_bar[st]), ph ^ 1u, p.timeout_ns)) {
@@ -805,10 +815,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     constexpr int KT = D / 16;  // k-steps of QK (f16/bf16 path)
     constexpr int MT = D / 16;  // m-tiles of PV
     uint32_t qf[KT][NT][2];
+    // E4M3 K/V with bf16 q: q enters the f16 MMA scaled per head by a power
+    // of two; qd[n][r] undoes it for score column 2c + r of head tile n.
+    float qd[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) qd[n][0] = qd[n][1] = 1.f;
     float o[MT][NT][4];
     float mrow[NT][2], lrow[NT][2];
     const float scale_log2 = p.scale_log2;
 
+    if (p.stall_role == 2) {
+        // Test hook: slow consumers.  Hold the first stage (the producer
+        // cannot refill it before it is released) for stall_ns.
+        if (mbar_wait_bounded(smem_u32(&full_bar[0]), 0, p.timeout_ns)) idle_ns(p.stall_ns);
+    }
     int st = 0;
     uint32_t ph = 0;
     while (true) {
@@ -844,20 +864,66 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     // f16 fragments in the E4M3 k-order: k-step ks covers
                     // d = 32*(ks/2) + 16*(ks%2) + {4c..4c+3}.
                     const int row = n * 8 + g;
+                    const uint8_t *qrow = sb + 2 * Sh::KV_REGION + row * D * 2;
+                    if constexpr (QBF16) {
+                        // bf16 q into the f16 product.  Direct conversion is
+                        // exact for elements in [2^-17, 65504] and loses at
+                        // most 2^-25 below; it is kept when every element of
+                        // the head is below 2^15 and its largest is at least
+                        // 2^-3 (small elements then lose < 2^-22 of the
+                        // largest).  A head tile with any other head is
+                        // redone with a per-head power of two 2^e that brings
+                        // each head's largest |q| into [2^14, 2^15): every
+                        // element within 2^31 of it is then exact (8
+                        // significant bits into 11), smaller ones lose less
+                        // than 2^-39 of it, and the scores get 2^-e back.
+                        float amax = 0.f;  // this lane's elements of head row g
 #pragma unroll
-                    for (int ks = 0; ks < KT; ++ks) {
-                        const int d0 = 32 * (ks >> 1) + 16 * (ks & 1) + 4 * c;
-                        const uint2 raw = *reinterpret_cast<const uint2 *>(sb + 2 * Sh::KV_REGION + (row * D + d0) * 2);
-                        uint32_t w0, w1;
-                        if constexpr (QBF16) {
-                            w0 = pack_f16x2(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u));
-                            w1 = pack_f16x2(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
-                        } else {
-                            w0 = raw.x;
-                            w1 = raw.y;
+                        for (int ks = 0; ks < KT; ++ks) {
+                            const int d0 = 32 * (ks >> 1) + 16 * (ks & 1) + 4 * c;
+                            const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + d0 * 2);
+                            const float x0 = __uint_as_float(raw.x << 16), x1 = __uint_as_float(raw.x & 0xffff0000u);
+                            const float x2 = __uint_as_float(raw.y << 16), x3 = __uint_as_float(raw.y & 0xffff0000u);
+                            amax = fmaxf(fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1))), fmaxf(fabsf(x2), fabsf(x3)));
+                            qf[ks][n][0] = live_head ? pack_f16x2(x0, x1) : 0u;
+                            qf[ks][n][1] = live_head ? pack_f16x2(x2, x3) : 0u;
                         }
-                        qf[ks][n][0] = live_head ? w0 : 0u;
-                        qf[ks][n][1] = live_head ? w1 : 0u;
+                        // head row g is small when all four of its lanes are
+                        const unsigned small = __ballot_sync(0xffffffffu, !(amax >= 0.125f));
+                        const bool row_small = ((small >> (4 * g)) & 0xfu) == 0xfu;
+                        if (__any_sync(0xffffffffu, live_head && (amax >= 32768.f || row_small))) {
+                            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                            // e = 141 - biased exponent of amax, kept in
+                            // [-126, 126] so that 2^e and 2^-e are normal
+                            const int be = (int)((__float_as_uint(amax) >> 23) & 0xffu);
+                            const int e = (live_head && amax > 0.f) ? max(-126, min(126, 141 - be)) : 0;
+                            const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+                            const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+                            qd[n][0] = __shfl_sync(0xffffffffu, down, 8 * c);      // head 2c
+                            qd[n][1] = __shfl_sync(0xffffffffu, down, 8 * c + 4);  // head 2c + 1
+#pragma unroll
+                            for (int ks = 0; ks < KT; ++ks) {
+                                const int d0 = 32 * (ks >> 1) + 16 * (ks & 1) + 4 * c;
+                                const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + d0 * 2);
+                                const uint32_t w0 = pack_f16x2(__uint_as_float(raw.x << 16) * up,
+                                                               __uint_as_float(raw.x & 0xffff0000u) * up);
+                                const uint32_t w1 = pack_f16x2(__uint_as_float(raw.y << 16) * up,
+                                                               __uint_as_float(raw.y & 0xffff0000u) * up);
+                                qf[ks][n][0] = live_head ? w0 : 0u;
+                                qf[ks][n][1] = live_head ? w1 : 0u;
+                            }
+                        } else {
+                            qd[n][0] = qd[n][1] = 1.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < KT; ++ks) {
+                            const int d0 = 32 * (ks >> 1) + 16 * (ks & 1) + 4 * c;
+                            const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + d0 * 2);
+                            qf[ks][n][0] = live_head ? raw.x : 0u;
+                            qf[ks][n][1] = live_head ? raw.y : 0u;
+                        }
                     }
                 }
             }
@@ -952,10 +1018,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 const bool v0 = g >= ll[sub] && g < nl[sub], v1 = (g + 8) >= ll[sub] && (g + 8) < nl[sub];
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
-                    sv[sub][n][0] = v0 ? (sv[sub][n][0] + s2[n][0]) * sc : -INFINITY;
-                    sv[sub][n][1] = v0 ? (sv[sub][n][1] + s2[n][1]) * sc : -INFINITY;
-                    sv[sub][n][2] = v1 ? (sv[sub][n][2] + s2[n][2]) * sc : -INFINITY;
-                    sv[sub][n][3] = v1 ? (sv[sub][n][3] + s2[n][3]) * sc : -INFINITY;
+                    float sc0 = sc, sc1 = sc;
+                    if constexpr (FP8 && QBF16) {
+                        sc0 *= qd[n][0];
+                        sc1 *= qd[n][1];
+                    }
+                    sv[sub][n][0] = v0 ? (sv[sub][n][0] + s2[n][0]) * sc0 : -INFINITY;
+                    sv[sub][n][1] = v0 ? (sv[sub][n][1] + s2[n][1]) * sc1 : -INFINITY;
+                    sv[sub][n][2] = v1 ? (sv[sub][n][2] + s2[n][2]) * sc0 : -INFINITY;
+                    sv[sub][n][3] = v1 ? (sv[sub][n][3] + s2[n][3]) * sc1 : -INFINITY;
                 }
             }
 

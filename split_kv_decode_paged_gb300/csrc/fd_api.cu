@@ -76,6 +76,14 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s limit on any device-side 
 constexpr double kItemOverheadTokens = 48.0;
 constexpr int kDefaultSplitMarginPct = 2;
 
+// Wait limit (>= 0; 0 = kTimeoutNs) and the stall test hook: off, or a
+// role of 1 or 2 with an idle time of at most one second.
+bool hooks_valid(int timeout_us, int stall_us, int stall_role) {
+    if (timeout_us < 0 || stall_us < 0 || stall_us > 1000000) return false;
+    if (stall_role < 0 || stall_role > 2) return false;
+    return stall_role == 0 ? stall_us == 0 : stall_us > 0;
+}
+
 int elem_bytes(fd_dtype t) { return t == FD_E4M3 ? 1 : (t == FD_F32 ? 4 : 2); }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -276,11 +284,12 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (!plan || !seq_lens_host) return FD_ERR_INVALID_ARG;
     fd_status st = validate_problem(problem);
     if (st != FD_OK) return st;
-    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0, 0};
+    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0};
     if (options) opt = *options;
     if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 ||
         opt.split_margin_pct < 0 || opt.split_margin_pct > 100 ||
-        (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128 && opt.tile_tokens != 256))
+        (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128 && opt.tile_tokens != 256) ||
+        !hooks_valid(opt.timeout_us, opt.debug_stall_us, opt.debug_stall_role))
         return FD_ERR_INVALID_ARG;
     // shared_kv: every q sequence attends KV row 0 (one block-table row, one
     // seq_lens entry): the B*G q rows of a KV head are sliced into items.
@@ -370,6 +379,9 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     plan->kv_rows = kv_rows;
     plan->row_fold = fold;
     plan->head_subgroups = nhg;
+    plan->timeout_us = opt.timeout_us;
+    plan->debug_stall_us = opt.debug_stall_us;
+    plan->debug_stall_role = opt.debug_stall_role;
     const size_t rows = (size_t)p.B * p.Hq;
     size_t off = 0;
     plan->ws_partial_o = off;
@@ -409,7 +421,8 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     if (plan->head_subgroups != ((p.Hq / p.Hkv) * fold + 8 * ks.nt - 1) / (8 * ks.nt)) return FD_ERR_INVALID_ARG;
     if (plan->tile_tokens != ks.tile || plan->chunk_tokens < ks.tile || plan->chunk_tokens % ks.tile != 0 ||
         plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->stages < kMinStages ||
-        plan->stages > kMaxStages || plan->grid_ctas < 1)
+        plan->stages > kMaxStages || plan->grid_ctas < 1 ||
+        !hooks_valid(plan->timeout_us, plan->debug_stall_us, plan->debug_stall_role))
         return FD_ERR_INVALID_ARG;
 
     const int boxr = std::gcd(p.page_size, ks.tile);
@@ -456,7 +469,9 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     dp.fuse_merge = plan->fuse_merge;
     dp.stages = plan->stages;
     dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
-    dp.timeout_ns = kTimeoutNs;
+    dp.timeout_ns = plan->timeout_us > 0 ? (uint64_t)plan->timeout_us * 1000ull : kTimeoutNs;
+    dp.stall_ns = (uint64_t)plan->debug_stall_us * 1000ull;
+    dp.stall_role = plan->debug_stall_role;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_decode(p, ks, dp, tmk, tmv, plan->grid_ctas, (size_t)plan->smem_bytes, s);

@@ -54,7 +54,9 @@ struct DecodeParams {
     int fuse_merge;
     int stages;
     float scale_log2;          // log2(e) / sqrt(D)
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;       // limit of every device-side wait
+    uint64_t stall_ns;         // test hook (0 = off): idle time of stall_role
+    int stall_role;            // 1: producer before its first load; 2: consumers before the first release
 };
 
 struct MergeParams {

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(fdlib):
     assert {"fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string"} <= declared
     for name in declared:
         assert hasattr(fdlib, name), name
-    assert _lib.fd_api_version() == 1
+    assert _lib.fd_api_version() == 2
 
 
 def test_status_strings(fdlib):
@@ -96,3 +96,48 @@ def test_decode_rejects_before_launch(fdlib):
     p8 = _prob(kv_dtype=torch.float8_e4m3fn)
     assert L.fd_append_kv(ctypes.byref(p8), fake, fake, fake, fake, None, None, fake, fake, None,
                           None) == _lib.FD_ERR_INVALID_ARG
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of fd_problem, fd_plan_options, fd_plan_t and
+    fd_host_io_layout have the C structs' sizes and field offsets (checked
+    against the header compiled by the host C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    structs = {"fd_problem": _lib.FdProblem, "fd_plan_options": _lib.FdPlanOptions, "fd_plan_t": _lib.FdPlan,
+               "fd_host_io_layout": _lib.FdHostIoLayout}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "fd_api.h"', 'int main(void) {']
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    for line in filter(None, got):
+        cname, fname, val = line.split()
+        py = structs[cname]
+        want = ctypes.sizeof(py) if fname == "size" else getattr(py, fname).offset
+        assert int(val) == want, (cname, fname, int(val), want)
+
+
+@pytest.mark.parametrize("kw", [dict(timeout_us=-1), dict(debug_stall_us=10), dict(debug_stall_role=1),
+                                dict(debug_stall_role=3, debug_stall_us=10),
+                                dict(debug_stall_role=1, debug_stall_us=2000000)])
+def test_plan_rejects_bad_timeout_options(fdlib, kw):
+    with pytest.raises(_lib.FdError) as ei:
+        _lib.fd_plan(_prob(), [10, 20], num_sms=148, **kw)
+    assert ei.value.code == _lib.FD_ERR_INVALID_ARG
+
+
+def test_plan_carries_timeout_options(fdlib):
+    plan = _lib.fd_plan(_prob(), [10, 20], num_sms=148, timeout_us=300, debug_stall_us=5000, debug_stall_role=2)
+    assert (plan.timeout_us, plan.debug_stall_us, plan.debug_stall_role) == (300, 5000, 2)
+    plan = _lib.fd_plan(_prob(), [10, 20], num_sms=148)
+    assert (plan.timeout_us, plan.debug_stall_us, plan.debug_stall_role) == (0, 0, 0)
