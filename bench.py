@@ -11,7 +11,11 @@ of 2x the L2 size) outside that step's event pair.  Prints ONE JSON line
 
 metric: achieved HBM GB/s of the decode call = algorithmic bytes (K+V of the
 live tokens, q, out, lse, live block-table entries, seq_lens, FP8 scales) /
-device time; us per call is reported beside it.
+device time; us per call is reported beside it.  The headline workload is the
+Llama-3-8B-shaped GQA batch; at one GPU the line also carries `per_config`:
+all five workloads (tiny MHA, single-sequence MHA, GQA batch, 131k-token long
+context, mixed FP8 batch) with us per call, GB/s, fraction of the measured
+copy peak, the plan, and the fp64 oracle timed on the host cores beside each.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (seed
 offset by rank, no collective on the data path: weak scaling) and value =
@@ -69,20 +73,19 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload_tag):
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, or None if absent or taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", f"fd_split_kv_decode_kernel_{workload_tag}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per launch of the decode kernel for a workload, from the
+    committed ncu summary profiles/decode_traffic.json, or None when absent
+    or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)["workloads"][workload_tag]
+    except Exception:
         return None
-    vals = {}
-    for line in open(path):
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if entry.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
-        return int(float(vals["dram_bytes_per_launch"]))
+        return int(entry["dram_bytes_per_launch"])
     except Exception:
         return None
 
@@ -607,6 +610,85 @@ def bench_merge(args):
         "gpu_launches_per_call": 1}))
 
 
+# ------------------------------------------------------------ per config
+CONFIG_TAGS = {1: "tiny_mha", 2: "single_seq_mha", 3: "gqa_batch", 4: "long_context", 5: "mixed_fp8"}
+
+
+def spread(ms):
+    """Median, p10 and p90 in microseconds of per-call times in ms."""
+    srt = sorted(ms)
+    return (statistics.median(srt) * 1e3, srt[len(srt) // 10] * 1e3, srt[(len(srt) * 9) // 10] * 1e3)
+
+
+def per_call_spread(wl, dec, calls=50):
+    """Per-call event pairs around each call, no flush in between (inputs
+    larger than 2x L2: one call's K/V stream evicts the previous one's).  An
+    event pair per call breaks the launch overlap of consecutive calls, so
+    these times run a few microseconds above the back-to-back mean."""
+    out = torch.empty_like(wl.q)
+    lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=wl.q.device)
+    args = (wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens)
+    kw = dict(k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse)
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        dec(*args, **kw)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    for a, b in ev:
+        a.record(st)
+        dec(*args, **kw)
+        b.record(st)
+    torch.cuda.synchronize()
+    dec.check()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def config_entry(cfg, wl, ms, dec, peak, flushed, cpu=None, spread_ms=None):
+    from split_kv_decode_paged_gb300 import workloads as W
+    spec = W.CONFIGS[cfg]
+    nbytes = W.algorithmic_bytes(spec, wl.seq_lens.cpu())
+    us = statistics.mean(ms) * 1e3
+    gbs = nbytes / us / 1e3
+    plan = dec.plan
+    e = {"workload": f"{spec.name}: B={spec.B}, Hq={spec.Hq}, Hkv={spec.Hkv}, D={spec.D}, {spec.kv} K/V, "
+                     f"{spec.page_size}-token pages, lengths {tuple(spec.lens)} (seed {W.config_seed(cfg)})",
+         "us_per_call": us, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak,
+         "timing": ("L2 flushed before every call, per-call event pairs (mean)" if flushed else
+                    "back to back, one event pair (mean)"),
+         "traffic": profiled_traffic(CONFIG_TAGS[cfg]),
+         "plan": {"num_splits": plan.num_splits, "chunk_tokens": plan.chunk_tokens, "tile_tokens": plan.tile_tokens,
+                  "stages": plan.stages, "grid_ctas": plan.grid_ctas, "work_items": plan.work_items_hint}}
+    sp = spread(ms if flushed else (spread_ms or []) or ms)
+    e["us_median"], e["us_p10"], e["us_p90"] = sp
+    if not flushed:
+        e["spread_timing"] = "per-call event pairs, no flush (inputs > 2x L2)"
+    if cpu is not None:
+        e["oracle"] = {"us_per_call": cpu["us_per_call"], "gbs": cpu["value"], "cores": cpu["cores"],
+                       "sample": cpu["sample"]}
+    return e
+
+
+def per_config_block(args, dev, peak, flush_buf, flush_bytes, headline):
+    """Every workload at one GPU, with the fp64 oracle timed on the host cores
+    beside it (a bounded sample of each, scaled to one call)."""
+    from split_kv_decode_paged_gb300 import workloads as W
+    per = {}
+    for c in (1, 2, 3, 4, 5):
+        if c == args.config:
+            wl, ms, dec, sp = headline
+        else:
+            wl = W.make_config(c, dev)
+            big = W.algorithmic_bytes(W.CONFIGS[c], wl.seq_lens.cpu()) > flush_bytes
+            ms, dec = time_decode(wl, 100 if big else 200, args.warmup, None if big else flush_buf)
+            sp = per_call_spread(wl, dec) if big else None
+        big = W.algorithmic_bytes(W.CONFIGS[c], wl.seq_lens.cpu()) > flush_bytes
+        cpu = None if args.no_cpu_baseline else cpu_baseline(wl.to("cpu"), target_s=args.per_config_cpu_seconds)
+        per[str(c)] = config_entry(c, wl, ms, dec, peak, not big, cpu, sp)
+        if c != args.config:
+            del wl, dec
+            torch.cuda.empty_cache()
+    return per
+
+
 # ------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -615,7 +697,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=HEADLINE_CONFIG)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--all-configs", action="store_true", help="also report every workload (per_config)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block (every workload, with the oracle timed beside it)")
+    ap.add_argument("--all-configs", action="store_true", help=argparse.SUPPRESS)  # the default now
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge", "ex", "large"],
@@ -638,7 +723,7 @@ def main():
     from split_kv_decode_paged_gb300 import workloads as W
     ws, rank, local = dist_env()
     spec = W.CONFIGS[args.config]
-    tag = {1: "tiny_mha", 2: "single_seq_mha", 3: "gqa_batch", 4: "long_context", 5: "mixed_fp8"}[args.config]
+    tag = CONFIG_TAGS[args.config]
     config = {"workload": f"{spec.name} (config {args.config})", "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv,
               "D": spec.D, "page_size": spec.page_size, "kv_dtype": spec.kv, "q_dtype": spec.q,
               "lengths": list(spec.lens), "l2": "flushed before every timed call (2x L2 write)"}
@@ -705,18 +790,18 @@ def main():
     total_ms = sum(ms)
     elapsed_s, bytes_all = aggregate(total_ms / 1e3, bytes_call * args.steps)
     value = bytes_all / elapsed_s / 1e9
-    med = statistics.median(ms)
-    srt = sorted(ms)
     peak, peak_kind = measured_peak()
     achieved = bytes_call / (total_ms / args.steps * 1e-3) / 1e9
     ms_flushed = None
     if big and not args.quick:
         ms_f, _ = time_decode(wl, min(args.steps, 50), 3, flush_buf)
         ms_flushed = sum(ms_f) / len(ms_f)
+    spread_ms = per_call_spread(wl, dec) if big and not args.quick else None
     if args.quick:
         warm_ms = graph_ms = float("nan")
         e2e_s, h2d, d2h = float("nan"), 0, 0
         args.no_cpu_baseline = True
+        args.no_per_config = True
     else:
         warm_ms, graph_ms = time_warm_and_graph(wl, dec)
         e2e_s, h2d, d2h = time_e2e(wl, dec, max(10, args.steps // 2))
@@ -724,9 +809,13 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "us_per_call": total_ms / args.steps * 1e3,
-        # per-call spread exists only when every call has its own event pair
-        "us_median": None if big else med * 1e3, "us_p10": None if big else srt[len(srt) // 10] * 1e3,
-        "us_p90": None if big else srt[(len(srt) * 9) // 10] * 1e3,
+        # per-call spread: the flushed calls' own event pairs, or (inputs
+        # larger than 2x L2) a second pass with an event pair around each call
+        **dict(zip(("us_median", "us_p10", "us_p90"),
+                   spread(ms) if not big else (spread(spread_ms) if spread_ms else (None, None, None)))),
+        "us_spread_timing": ("per-call event pairs after an L2 flush" if not big else
+                             "second pass: per-call event pairs, no flush (inputs > 2x L2); the event pair per "
+                             "call breaks the launch overlap, so these run above the back-to-back mean"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16", "f16": "f16", "e4m3": "e4m3 (f16 MMA, fp32 accumulate)"}[spec.kv],
         "data": "synthetic (seeded generator: split_kv_decode_paged_gb300/workloads.py)", "config": config,
@@ -749,21 +838,8 @@ def main():
         "gpu_launches": args.steps * (1 if plan.fuse_merge or plan.num_splits == 1 else 2),
         "clocks": clk.summary(), "wall_s_timed_region": wall,
     }
-    if args.all_configs and rank == 0:
-        per = {}
-        for c in (1, 2, 3, 4, 5):
-            if c == args.config:
-                per[c] = {"us": total_ms / args.steps * 1e3, "gbs": achieved, "frac": achieved / peak}
-                continue
-            w2 = W.make_config(c, dev)
-            b2 = W.algorithmic_bytes(W.CONFIGS[c], w2.seq_lens.cpu())
-            ms2, d2 = time_decode(w2, 30, 3, None if b2 > flush_bytes else flush_buf)
-            t2 = sum(ms2) / len(ms2)
-            per[c] = {"us": t2 * 1e3, "gbs": b2 / (t2 * 1e-3) / 1e9, "frac": b2 / (t2 * 1e-3) / 1e9 / peak,
-                      "splits": d2.plan.num_splits, "chunk": d2.plan.chunk_tokens}
-            del w2, d2
-            torch.cuda.empty_cache()
-        line["per_config"] = per
+    if ws == 1 and not args.no_per_config:
+        line["per_config"] = per_config_block(args, dev, peak, flush_buf, flush_bytes, (wl, ms, dec, spread_ms))
     if rank == 0 and not args.no_cpu_baseline:
         wl_cpu = wl.to("cpu")
         line["cpu_baseline"] = cpu_baseline(wl_cpu, target_s=args.cpu_seconds)
