@@ -9,6 +9,10 @@ cudaError_t launch_decode_bf16(const fd_problem &p, const KernelShape &ks, const
     return launch_decode_kind<KV_BF16, true>(p, ks, dp, tmk, tmv, grid, smem, stream);
 }
 
+cudaError_t decode_occupancy_bf16(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks) {
+    return occupancy_kind<KV_BF16, true>(p, ks, smem, blocks);
+}
+
 size_t decode_smem_bf16(const fd_problem &p, const KernelShape &ks, int stages) {
     return decode_smem_kind<KV_BF16, false>(p, ks, stages);
 }

@@ -25,6 +25,25 @@ cudaError_t launch_decode_d(const KernelShape &ks, const DecodeParams &dp, const
 }
 
 template <int KV, int D, int NT, bool QBF16>
+cudaError_t occupancy_d(const KernelShape &ks, size_t smem, int *blocks) {
+    if (ks.consumer_warps == 4 && ks.subtiles == 1) return occupancy_t<KV, D, NT, 4, 1, QBF16>(smem, blocks);
+    if constexpr (KV == KV_E4M3) {
+        if (ks.consumer_warps == 8 && ks.subtiles == 2) return occupancy_t<KV, D, NT, 8, 2, QBF16>(smem, blocks);
+    }
+    if (ks.consumer_warps == 8 && ks.subtiles == 1) return occupancy_t<KV, D, NT, 8, 1, QBF16>(smem, blocks);
+    return cudaErrorInvalidValue;
+}
+
+template <int KV, bool QBF16>
+cudaError_t occupancy_kind(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks) {
+    if (p.D == 128)
+        return ks.nt == 1 ? occupancy_d<KV, 128, 1, QBF16>(ks, smem, blocks) : occupancy_d<KV, 128, 2, QBF16>(ks, smem, blocks);
+    if (p.D == 64)
+        return ks.nt == 1 ? occupancy_d<KV, 64, 1, QBF16>(ks, smem, blocks) : occupancy_d<KV, 64, 2, QBF16>(ks, smem, blocks);
+    return cudaErrorInvalidValue;
+}
+
+template <int KV, int D, int NT, bool QBF16>
 size_t decode_smem_d(const KernelShape &ks, int stages, int B) {
     if (ks.consumer_warps == 4 && ks.subtiles == 1) return decode_smem_for<KV, D, NT, 4, 1, QBF16>(stages, B);
     if (ks.consumer_warps == 8 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 8, 2, QBF16>(stages, B);

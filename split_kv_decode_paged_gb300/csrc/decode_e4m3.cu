@@ -10,6 +10,11 @@ cudaError_t launch_decode_e4m3(const fd_problem &p, const KernelShape &ks, const
     return launch_decode_kind<KV_E4M3, false>(p, ks, dp, tmk, tmv, grid, smem, stream);
 }
 
+cudaError_t decode_occupancy_e4m3(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks) {
+    if (p.q_dtype == FD_BF16) return occupancy_kind<KV_E4M3, true>(p, ks, smem, blocks);
+    return occupancy_kind<KV_E4M3, false>(p, ks, smem, blocks);
+}
+
 size_t decode_smem_e4m3(const fd_problem &p, const KernelShape &ks, int stages) {
     return decode_smem_kind<KV_E4M3, false>(p, ks, stages);
 }

@@ -9,6 +9,10 @@ cudaError_t launch_decode_f16(const fd_problem &p, const KernelShape &ks, const 
     return launch_decode_kind<KV_F16, false>(p, ks, dp, tmk, tmv, grid, smem, stream);
 }
 
+cudaError_t decode_occupancy_f16(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks) {
+    return occupancy_kind<KV_F16, false>(p, ks, smem, blocks);
+}
+
 size_t decode_smem_f16(const fd_problem &p, const KernelShape &ks, int stages) {
     return decode_smem_kind<KV_F16, false>(p, ks, stages);
 }

@@ -1367,6 +1367,16 @@ size_t decode_smem_for(int stages, int B) {
     return n;
 }
 
+// Resident CTAs per SM of this instance with `smem` bytes of dynamic shared
+// memory (registers, threads and shared memory all counted).
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
+cudaError_t occupancy_t(size_t smem, int *blocks) {
+    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, kern, DecodeShape<KV, D, NT, NC, SUBT>::THREADS, smem);
+}
+
 template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
 cudaError_t launch_decode_t(const DecodeParams &dp, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                             size_t smem, cudaStream_t stream) {

@@ -19,6 +19,9 @@ cudaError_t launch_decode_bf16(const fd_problem &, const KernelShape &, const De
                                const CUtensorMap &, int, size_t, cudaStream_t);
 cudaError_t launch_decode_e4m3(const fd_problem &, const KernelShape &, const DecodeParams &, const CUtensorMap &,
                                const CUtensorMap &, int, size_t, cudaStream_t);
+cudaError_t decode_occupancy_f16(const fd_problem &, const KernelShape &, size_t, int *);
+cudaError_t decode_occupancy_bf16(const fd_problem &, const KernelShape &, size_t, int *);
+cudaError_t decode_occupancy_e4m3(const fd_problem &, const KernelShape &, size_t, int *);
 size_t decode_smem_f16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
@@ -52,6 +55,14 @@ size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages)
     }
 }
 
+cudaError_t decode_occupancy(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks) {
+    switch (p.kv_dtype) {
+    case FD_F16: return decode_occupancy_f16(p, ks, smem, blocks);
+    case FD_BF16: return decode_occupancy_bf16(p, ks, smem, blocks);
+    default: return decode_occupancy_e4m3(p, ks, smem, blocks);
+    }
+}
+
 cudaError_t launch_decode(const fd_problem &p, const KernelShape &ks, const DecodeParams &dp, const CUtensorMap &tmk,
                           const CUtensorMap &tmv, int grid, size_t smem, cudaStream_t stream) {
     switch (p.kv_dtype) {
@@ -75,6 +86,12 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s limit on any device-side 
 // fewer splits are preferred.
 constexpr double kItemOverheadTokens = 48.0;
 constexpr int kDefaultSplitMarginPct = 2;
+// Below this many attended tokens per work item on average (and with enough
+// items), the planner runs two CTAs per SM with 64-token stages; the higher
+// figure applies when the default shape has lost pipeline depth to large
+// dispatch tables (measured crossovers on GB300: ~700 and above 1024 tokens).
+constexpr double kShortItemTokens = 768.0;
+constexpr double kShortItemTokensShallow = 1280.0;
 
 // Wait limit (>= 0; 0 = kTimeoutNs) and the stall test hook: off, or a
 // role of 1 or 2 with an idle time of at most one second.
@@ -112,7 +129,9 @@ fd_status validate_problem(const fd_problem *p) {
 
 struct DeviceInfo {
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;     // per CTA (opt-in maximum)
+    int smem_per_sm = 0;    // per SM
+    int smem_reserved = 0;  // set aside per resident CTA
 };
 
 fd_status device_info(DeviceInfo &di) {
@@ -125,7 +144,9 @@ fd_status device_info(DeviceInfo &di) {
     if (cache[dev].sms == 0) {
         DeviceInfo d;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FD_ERR_CUDA;
-        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return FD_ERR_CUDA;
         cache[dev] = d;
     }
@@ -308,61 +329,114 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (capL > (long long)p.page_size * p.max_blocks_per_seq) return FD_ERR_INVALID_ARG;
 
     // The device is queried when present; planning for an explicit SM count
-    // also works on a host without a GPU (shared memory then assumes 227 KB).
+    // also works on a host without a GPU (shared memory then assumes GB300's
+    // 227 KB per CTA, 228 KB per SM, 1 KB reserved per CTA).
     DeviceInfo di;
     int sms = opt.num_sms;
-    int smem_optin = 232448;
     st = device_info(di);
-    if (st == FD_OK) smem_optin = di.smem_optin;
+    const bool have_dev = st == FD_OK;
+    if (!have_dev) {
+        di.smem_optin = 232448;
+        di.smem_per_sm = 233472;
+        di.smem_reserved = 1024;
+    }
     if (sms == 0) {
-        if (st != FD_OK) return st;
+        if (!have_dev) return st;
         sms = di.sms;
     }
-    // E4M3 pools default to 256-token stages (8 consumer warps x 2 sub-tiles)
-    // when the pages allow them and three stages fit; otherwise 128.
+    // Dynamic shared memory one CTA may take when cps CTAs share an SM.
+    auto smem_limit = [&](int cps) -> long long {
+        if (cps <= 1) return di.smem_optin;
+        return std::min<long long>(di.smem_optin, (di.smem_per_sm - (long long)cps * di.smem_reserved) / cps);
+    };
+
+    // One candidate kernel shape: stage size, CTAs per SM, chunk length,
+    // partial slots, work items and the deepest pipeline that fits.
+    struct Shape {
+        KernelShape ks;
+        int cps = 1, nhg = 1, C = 0, slots = 0, stages = 0;
+        size_t smem = 0;
+        long long items = 0;
+    };
+    auto make_shape = [&](int tile_opt, int cps, Shape &sh) -> bool {
+        sh.ks = kernel_shape(p, tile_opt, fold);
+        sh.cps = cps;
+        const int tile = sh.ks.tile;
+        const int qrows = 8 * sh.ks.nt;
+        sh.nhg = ((p.Hq / p.Hkv) * fold + qrows - 1) / qrows;
+        fd_problem pk = p;  // the KV side of the problem: kv_rows rows, nhg items per KV head
+        pk.B = kv_rows;
+        pk.Hkv = p.Hkv * sh.nhg;
+        const int P = sms * cps;
+        int C;
+        if (opt.num_splits > 0) {
+            const int S = std::min(opt.num_splits, kMaxSplits);
+            C = std::max(tile, round_up((std::max<long long>(maxL, 1) + S - 1) / S, tile));
+        } else {
+            C = choose_chunk(lens, pk, P, tile, margin);
+        }
+        int slots = (int)std::max<long long>(1, (capL + C - 1) / C);
+        if (slots > kMaxSplits) {
+            C = std::max(tile, round_up((capL + kMaxSplits - 1) / kMaxSplits, tile));
+            slots = (int)std::max<long long>(1, (capL + C - 1) / C);
+        }
+        sh.C = C;
+        sh.slots = slots;
+        sh.items = 0;
+        for (int L : lens) sh.items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv * sh.nhg;
+        sh.stages = 0;
+        for (int s = kMaxStages; s >= kMinStages; --s) {
+            const size_t need = decode_smem_bytes(p, sh.ks, s);
+            if ((long long)need <= smem_limit(cps)) {
+                sh.stages = s;
+                sh.smem = need;
+                break;
+            }
+        }
+        return sh.stages > 0;
+    };
+
+    // Default shape.  E4M3 pools take 256-token stages (8 consumer warps x 2
+    // sub-tiles) when the pages allow them and three stages fit; otherwise
+    // 128 (16-bit K/V: always 128).
+    const int cps_opt = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
     int tile_opt = opt.tile_tokens;
     if (tile_opt == 0 && p.kv_dtype == FD_E4M3) {
         const KernelShape k256 = kernel_shape(p, 256, fold);
-        if (k256.tile == 256 && (long long)decode_smem_bytes(p, k256, 3) <= smem_optin / std::max(1, opt.ctas_per_sm))
-            tile_opt = 256;
+        if (k256.tile == 256 && (long long)decode_smem_bytes(p, k256, 3) <= smem_limit(cps_opt)) tile_opt = 256;
     }
-    const KernelShape ks = kernel_shape(p, tile_opt, fold);
-    const int tile = ks.tile;
-    const int qrows = 8 * ks.nt;
-    const int nhg = ((p.Hq / p.Hkv) * fold + qrows - 1) / qrows;
-    fd_problem pk = p;  // the KV side of the problem: kv_rows rows, nhg items per KV head
-    pk.B = kv_rows;
-    pk.Hkv = p.Hkv * nhg;
-    const int ctas_per_sm = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
-    const int P = sms * ctas_per_sm;
-
-    int C;
-    if (opt.num_splits > 0) {
-        const int S = std::min(opt.num_splits, kMaxSplits);
-        C = std::max(tile, round_up((std::max<long long>(maxL, 1) + S - 1) / S, tile));
-    } else {
-        C = choose_chunk(lens, pk, P, tile, margin);
-    }
-    int slots = (int)std::max<long long>(1, (capL + C - 1) / C);
-    if (slots > kMaxSplits) {
-        C = std::max(tile, round_up((capL + kMaxSplits - 1) / kMaxSplits, tile));
-        slots = (int)std::max<long long>(1, (capL + C - 1) / C);
-    }
-    long long items = 0;
-    for (int L : lens) items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv * nhg;
-
-    // Deepest pipeline that fits in shared memory.
-    int stages = 0;
-    size_t smem = 0;
-    for (int s = kMaxStages; s >= kMinStages; --s) {
-        const size_t need = decode_smem_bytes(p, ks, s);
-        if ((long long)need <= smem_optin / ctas_per_sm) {
-            stages = s;
-            smem = need;
-            break;
+    Shape sh;
+    if (!make_shape(tile_opt, cps_opt, sh)) return FD_ERR_UNSUPPORTED;
+    // Many short work items: two CTAs per SM with 64-token stages, so one
+    // CTA streams while the other is between items (epilogue, next claim,
+    // page ids).  Taken when the shape is left to the planner, the average
+    // item attends fewer tokens than the threshold, there are enough items
+    // for both CTAs of every SM, and two CTAs of that shape fit on an SM.
+    if (opt.tile_tokens == 0 && opt.ctas_per_sm == 0 && sh.items >= 4LL * sms) {
+        long long tok = 0;
+        for (int L : lens) tok += L;
+        const double mean_item = (double)tok * p.Hkv * sh.nhg / (double)sh.items;
+        const bool shallow = sh.stages < 3 || (p.kv_dtype == FD_E4M3 && sh.ks.tile < 256);
+        Shape s2;
+        if (mean_item < (shallow ? kShortItemTokensShallow : kShortItemTokens) && make_shape(64, 2, s2)) {
+            bool fits = s2.ks.nt == 1 || p.D == 64;  // register budget of two 5-warp CTAs
+            if (have_dev) {
+                int blocks = 0;
+                fits = decode_occupancy(p, s2.ks, s2.smem, &blocks) == cudaSuccess && blocks >= 2;
+                cudaGetLastError();
+            }
+            if (fits) sh = s2;
         }
     }
-    if (stages == 0) return FD_ERR_UNSUPPORTED;
+    const KernelShape ks = sh.ks;
+    const int tile = ks.tile;
+    const int nhg = sh.nhg;
+    const int P = sms * sh.cps;
+    const int C = sh.C;
+    const int slots = sh.slots;
+    const long long items = sh.items;
+    const int stages = sh.stages;
+    const size_t smem = sh.smem;
 
     std::memset(plan, 0, sizeof(*plan));
     plan->problem = p;

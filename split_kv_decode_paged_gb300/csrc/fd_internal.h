@@ -102,6 +102,9 @@ struct KernelShape {
 KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold);
 size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages);
 int decode_max_stages(const fd_problem &p, const KernelShape &ks);
+// Resident CTAs per SM of the decode kernel of this shape with smem bytes of
+// dynamic shared memory (needs a device).
+cudaError_t decode_occupancy(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks);
 
 cudaError_t launch_decode(const fd_problem &p, const KernelShape &ks, const DecodeParams &dp,
                           const CUtensorMap &tmk, const CUtensorMap &tmv, int grid, size_t smem,

@@ -226,3 +226,21 @@ def test_many_splits_up_to_the_maximum(fdlib, L, splits, want, fuse):
     spec = _spec(f"L={L} S={splits}", 2, 8, 2, 64, 64, "bf16", "bf16", [L, L // 3])
     err, dec = _run_and_check(spec, 5 + splits, num_splits=splits, fuse_merge=fuse)
     assert dec.plan.num_splits == want
+
+
+@pytest.mark.parametrize("kv,q,ps,D", [("bf16", "bf16", 16, 128), ("e4m3", "bf16", 128, 128), ("f16", "f16", 32, 64),
+                                       ("e4m3", "f16", 64, 128)])
+def test_short_items_two_ctas_per_sm(fdlib, kv, q, ps, D):
+    """Many short sequences: the planner runs two CTAs per SM with 64-token
+    stages (4 consumer warps); every row against the oracle, with empty,
+    one-token and page-boundary lengths among them."""
+    rng = np.random.default_rng(31 + ps)
+    B = 700
+    lens = rng.integers(1, 700, B)
+    lens[::50] = 0
+    lens[1::50] = 1
+    lens[2::50] = ps
+    spec = _spec(f"short {kv}", B, 32, 8, D, ps, kv, q, lens.tolist())
+    err, dec = _run_and_check(spec, 17 + ps)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert dec.plan.tile_tokens == 64 and dec.plan.grid_ctas == 2 * sms

@@ -113,10 +113,53 @@ def test_head_subgroups_and_shared_kv(fdlib):
     (torch.bfloat16, 16, 8192, 0, 128, 2),         # the largest batch still plans
 ])
 def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
+    # items of 4000 tokens: long enough that the one-CTA-per-SM shape is kept
     prob = _lib.make_problem(B, 64, 8, 128, ps, 4096 // ps, B * (4096 // ps), torch.bfloat16, kv)
-    plan = _lib.fd_plan(prob, [1000] * B, num_sms=152, tile_tokens=tile_opt)
+    plan = _lib.fd_plan(prob, [4000] * B, num_sms=152, tile_tokens=tile_opt)
     assert plan.tile_tokens == want_tile
     assert plan.chunk_tokens % plan.tile_tokens == 0
     assert plan.smem_bytes <= 232448
     if want_stages is not None:
         assert plan.stages == want_stages
+
+
+SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per CTA
+
+
+@pytest.mark.parametrize("kv,ps,B,L,want_two", [
+    (torch.bfloat16, 16, 512, 256, True),      # short items: two CTAs per SM, 64-token stages
+    (torch.bfloat16, 16, 512, 512, True),
+    (torch.bfloat16, 16, 512, 1024, False),    # long enough for the default shape
+    (torch.bfloat16, 16, 2048, 1024, True),    # ... unless the default lost a stage to its tables
+    (torch.bfloat16, 16, 2048, 2048, False),
+    (torch.float8_e4m3fn, 128, 512, 512, True),
+    (torch.float8_e4m3fn, 128, 512, 1024, False),
+    (torch.float8_e4m3fn, 128, 2048, 1024, True),
+    (torch.bfloat16, 16, 16, 256, False),      # 128 items cannot fill two CTAs on every SM
+])
+def test_short_items_take_two_ctas_per_sm(kv, ps, B, L, want_two):
+    """The planner's shape for many short work items: 64-token stages with two
+    persistent CTAs per SM (one streams while the other is between items)."""
+    nb = 4096 // ps
+    prob = _lib.make_problem(B, 32, 8, 128, ps, nb, B * nb, torch.bfloat16, kv)
+    plan = _lib.fd_plan(prob, [L] * B, num_sms=152)
+    if want_two:
+        assert plan.tile_tokens == 64 and plan.grid_ctas == 2 * 152 and plan.stages >= 2
+        assert plan.smem_bytes <= (SM_SMEM - 2 * RESERVED) // 2
+    else:
+        assert plan.tile_tokens >= 128 and plan.grid_ctas <= 152
+
+
+def test_short_items_rule_respects_explicit_options_and_registers(fdlib):
+    prob = _lib.make_problem(512, 32, 8, 128, 16, 64, 512 * 64, torch.bfloat16, torch.bfloat16)
+    assert _lib.fd_plan(prob, [256] * 512, num_sms=152, tile_tokens=128).tile_tokens == 128
+    p1 = _lib.fd_plan(prob, [256] * 512, num_sms=152, ctas_per_sm=1)
+    assert p1.grid_ctas <= 152
+    # 16 query heads per KV head at D = 128: two 5-warp CTAs do not fit the
+    # register file, so the one-CTA shape stays
+    prob16 = _lib.make_problem(512, 128, 8, 128, 16, 64, 512 * 64, torch.bfloat16, torch.bfloat16)
+    p16 = _lib.fd_plan(prob16, [256] * 512, num_sms=152)
+    assert p16.grid_ctas <= 152 and p16.tile_tokens == 128
+    # the same at D = 64 does fit
+    prob64 = _lib.make_problem(512, 128, 8, 64, 16, 64, 512 * 64, torch.bfloat16, torch.bfloat16)
+    assert _lib.fd_plan(prob64, [256] * 512, num_sms=152).grid_ctas == 304
