@@ -798,10 +798,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         } else {
             flag_status(p.status, FD_DEV_TIMEOUT);
         }
-        // Last producer out resets the work counters for the next launch.
+        // Last producer out resets the work counters for the next launch
+        // (the release orders this CTA's claims before its count; the
+        // acquire orders every CTA's claims before the reset).
         if (lane == 0) {
-            __threadfence();
-            const int done = atomicAdd(p.done_ctr, 1);
+            const int done = atom_add_acq_rel_gpu(p.done_ctr, 1);
             if (done == (int)gridDim.x - 1) {
                 atomicExch(p.work_ctr, 0);
                 atomicExch(p.done_ctr, 0);
@@ -1335,14 +1336,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         if (m_nsplit > 1 && p.fuse_merge) {
             // Publish the partial state: the barrier orders every consumer
-            // thread's stores before thread 0's device-scope fence and
-            // counter update (release); the CTA that sees the last count
-            // fences again (acquire) before reading the other partials.
+            // thread's stores before thread 0's GPU-scope counter update,
+            // whose release makes them visible to the other CTAs; its
+            // acquire makes theirs visible to the CTA that sees the last
+            // count (the barrier below passes that on to its threads).
             named_bar_sync(1, NC * 32);
             if (tid == 0) {
-                __threadfence();
-                const int prev = atomicAdd(p.merge_ctr + ((size_t)mb * p.Hkv + m_kvh) * p.nhg + m_hg, 1);
-                __threadfence();
+                const int prev = atom_add_acq_rel_gpu(p.merge_ctr + ((size_t)mb * p.Hkv + m_kvh) * p.nhg + m_hg, 1);
                 *scr_flag = (prev == m_nsplit - 1);
             }
             named_bar_sync(1, NC * 32);

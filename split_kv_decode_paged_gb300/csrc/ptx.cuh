@@ -111,6 +111,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Atomic add at GPU scope with acquire-release ordering: the writes this
+// thread has made or observed (e.g. its CTA's, ordered by a barrier) are
+// visible before the add, and writes released by earlier adds are visible
+// after it.  Returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // --------------------------------------------- programmatic dependent launch
 // Wait until the preceding grid in the stream (if it was launched with a
 // programmatic dependency on us) has completed and its writes are visible.
