@@ -85,6 +85,10 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s limit on any device-side 
 // item (epilogue + pipeline hand-over) and the relative margin within which
 // fewer splits are preferred.
 constexpr double kItemOverheadTokens = 48.0;
+// Extra CTA time of an item of a split sequence: publishing its partial
+// state and the fused merge, measured at ~1.6 us, i.e. the bytes one CTA
+// streams in that time (~45 GB/s per CTA).
+constexpr double kSplitPublishBytes = 73728.0;
 constexpr int kDefaultSplitMarginPct = 2;
 // Below this many attended tokens per work item on average (and with enough
 // items), the planner runs two CTAs per SM with 64-token stages; the higher
@@ -159,20 +163,24 @@ int round_up(long long x, int a) { return (int)(((x + a - 1) / a) * a); }
 // Greedy list-scheduling estimate of the busiest CTA (in token-times) when
 // the items of chunk length C are handed out to P CTAs in the kernel's
 // dispatch order: every full chunk first, then each sequence's partial
-// chunk, longest first (Hkv items per chunk).
-double makespan(const std::vector<int> &lens, int Hkv, int C, int P, double item_ovh) {
-    std::vector<int> items;
-    std::vector<int> tails;
+// chunk, longest first (Hkv items per chunk).  Every item costs item_ovh
+// more, and every item of a split sequence (L > C) split_ovh more again.
+double makespan(const std::vector<int> &lens, int Hkv, int C, int P, double item_ovh, double split_ovh) {
+    std::vector<double> items;
+    std::vector<std::pair<int, double>> tails;
     for (int L : lens) {
-        for (int s = 0; s < L / C; ++s) items.push_back(C);
-        if (L == 0 || L % C) tails.push_back(L % C);
+        const double extra = L > C ? split_ovh : 0.0;
+        for (int s = 0; s < L / C; ++s) items.push_back(C + extra);
+        if (L == 0 || L % C) tails.push_back({L % C, extra});
     }
-    std::stable_sort(tails.begin(), tails.end(), [](int a, int b) { return a > b; });
-    items.insert(items.end(), tails.begin(), tails.end());
+    std::stable_sort(tails.begin(), tails.end(), [](const std::pair<int, double> &a, const std::pair<int, double> &b) {
+        return a.first > b.first;
+    });
+    for (const auto &t : tails) items.push_back(t.first + t.second);
     std::priority_queue<double, std::vector<double>, std::greater<double>> q;
     for (int i = 0; i < P; ++i) q.push(0.0);
     double worst = 0.0;
-    for (int len : items) {
+    for (double len : items) {
         for (int h = 0; h < Hkv; ++h) {
             double t = q.top();
             q.pop();
@@ -211,7 +219,8 @@ int choose_chunk(const std::vector<int> &lens, const fd_problem &p, int P, int t
         for (int L : lens) items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv;
         if (S > 1 && items > 16LL * P) continue;
         const int nmax = (maxL + C - 1) / C;
-        double cost = makespan(lens, p.Hkv, C, P, kItemOverheadTokens);
+        const double split_ovh = kSplitPublishBytes / (2.0 * p.D * elem_bytes(p.kv_dtype));
+        double cost = makespan(lens, p.Hkv, C, P, kItemOverheadTokens, split_ovh);
         if (nmax > 1) cost += 0.5 * G * nmax;  // merge of nmax partials by one CTA
         opts.push_back({S, C, cost});
     }
