@@ -143,10 +143,11 @@ typedef struct {
     int kv_rows;          /* block-table / seq_lens rows the call reads          */
     int row_fold;         /* q sequences per KV row (1, or B with shared_kv)     */
     int head_subgroups;   /* work items per (KV row, split, KV head)             */
+    int ctas_per_sm;      /* persistent CTAs per SM the shape was chosen for     */
     int timeout_us;       /* device wait limit (0 = 2 s), from the options       */
     int debug_stall_us;   /* test hook copied from the options (0 = off)         */
     int debug_stall_role;
-    int reserved[2];
+    int reserved[1];
 } fd_plan_t;
 
 /* Plan a decode call [P1 §2.1 step 1; P2 进阶突破; P3 §6.3, §8.2].

@@ -65,8 +65,8 @@ class FdPlan(ctypes.Structure):
                 ("ws_partial_o", ctypes.c_size_t), ("ws_partial_md", ctypes.c_size_t),
                 ("ws_counters", ctypes.c_size_t), ("work_items_hint", ctypes.c_longlong),
                 ("kv_rows", ctypes.c_int), ("row_fold", ctypes.c_int), ("head_subgroups", ctypes.c_int),
-                ("timeout_us", ctypes.c_int), ("debug_stall_us", ctypes.c_int), ("debug_stall_role", ctypes.c_int),
-                ("reserved", ctypes.c_int * 2)]
+                ("ctas_per_sm", ctypes.c_int), ("timeout_us", ctypes.c_int), ("debug_stall_us", ctypes.c_int),
+                ("debug_stall_role", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n not in ("problem", "reserved")}

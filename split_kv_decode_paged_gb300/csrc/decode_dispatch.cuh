@@ -6,7 +6,8 @@ namespace fd {
 
 // (consumer warps, sub-tiles per warp) pairs built for each storage kind:
 // 16-bit K/V: (4,1) = 64-token stages, (8,1) = 128-token stages;
-// E4M3 K/V:   (4,1) = 64-token stages, (8,1) = 128-token stages, (8,2) = 256-token stages.
+// E4M3 K/V:   (4,1) = 64-token stages, (8,1) = 128-token stages, (8,2) = 256-token stages,
+//             (4,2) = 128-token stages for two CTAs per SM.
 template <int KV, int D, int NT, bool QBF16>
 cudaError_t launch_decode_d(const KernelShape &ks, const DecodeParams &dp, const CUtensorMap &tmk,
                             const CUtensorMap &tmv, int grid, size_t smem, cudaStream_t stream) {
@@ -17,6 +18,8 @@ cudaError_t launch_decode_d(const KernelShape &ks, const DecodeParams &dp, const
             return launch_decode_t<KV, D, NT, 8, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);
         if (ks.consumer_warps == 8 && ks.subtiles == 2)
             return launch_decode_t<KV, D, NT, 8, 2, QBF16>(dp, tmk, tmv, grid, smem, stream);
+        if (ks.consumer_warps == 4 && ks.subtiles == 2)
+            return launch_decode_t<KV, D, NT, 4, 2, QBF16>(dp, tmk, tmv, grid, smem, stream);
     } else {
         if (ks.consumer_warps == 8 && ks.subtiles == 1)
             return launch_decode_t<KV, D, NT, 8, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);
@@ -29,6 +32,7 @@ cudaError_t occupancy_d(const KernelShape &ks, size_t smem, int *blocks) {
     if (ks.consumer_warps == 4 && ks.subtiles == 1) return occupancy_t<KV, D, NT, 4, 1, QBF16>(smem, blocks);
     if constexpr (KV == KV_E4M3) {
         if (ks.consumer_warps == 8 && ks.subtiles == 2) return occupancy_t<KV, D, NT, 8, 2, QBF16>(smem, blocks);
+        if (ks.consumer_warps == 4 && ks.subtiles == 2) return occupancy_t<KV, D, NT, 4, 2, QBF16>(smem, blocks);
     }
     if (ks.consumer_warps == 8 && ks.subtiles == 1) return occupancy_t<KV, D, NT, 8, 1, QBF16>(smem, blocks);
     return cudaErrorInvalidValue;
@@ -47,6 +51,7 @@ template <int KV, int D, int NT, bool QBF16>
 size_t decode_smem_d(const KernelShape &ks, int stages, int B) {
     if (ks.consumer_warps == 4 && ks.subtiles == 1) return decode_smem_for<KV, D, NT, 4, 1, QBF16>(stages, B);
     if (ks.consumer_warps == 8 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 8, 2, QBF16>(stages, B);
+    if (ks.consumer_warps == 4 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 4, 2, QBF16>(stages, B);
     return decode_smem_for<KV, D, NT, 8, 1, QBF16>(stages, B);
 }
 

@@ -26,7 +26,7 @@ size_t decode_smem_f16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int);
 size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
 
-KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold) {
+KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold, int ctas_per_sm) {
     KernelShape ks;
     // 256-token stages: E4M3 only, with pages of >= 32 tokens (at most
     // kMaxBoxesPerTile boxes per stage).
@@ -36,6 +36,11 @@ KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold) {
     if (tile == 64) {
         ks.consumer_warps = 4;
         ks.subtiles = 1;
+    } else if (tile == 128 && ctas_per_sm >= 2 && p.kv_dtype == FD_E4M3) {
+        // 4 consumer warps, 32 tokens each per 128 (two sub-tiles sharing one
+        // online-softmax step): the register budget of two CTAs per SM.
+        ks.consumer_warps = 4;
+        ks.subtiles = 2;
     } else {
         // 8 consumer warps, 16 tokens each per 128 (one sub-tile; E4M3 with
         // 256-token stages: two).
@@ -91,11 +96,15 @@ constexpr double kItemOverheadTokens = 48.0;
 constexpr double kSplitPublishBytes = 73728.0;
 constexpr int kDefaultSplitMarginPct = 2;
 // Below this many attended tokens per work item on average (and with enough
-// items), the planner runs two CTAs per SM with 64-token stages; the higher
-// figure applies when the default shape has lost pipeline depth to large
-// dispatch tables (measured crossovers on GB300: ~700 and above 1024 tokens).
+// items), the planner runs two CTAs per SM; for 16-bit K/V the higher figure
+// applies when the default shape has lost pipeline depth to large dispatch
+// tables (measured crossovers on GB300: ~700 and above 1024 tokens).  E4M3
+// K/V switch below 2048 tokens per item when the default shape has 256-token
+// stages, and always otherwise (16-token pages or very large batches, where
+// one producer per SM issuing 2 KB boxes is the limit).
 constexpr double kShortItemTokens = 768.0;
 constexpr double kShortItemTokensShallow = 1280.0;
+constexpr double kShortItemTokensE4m3 = 2048.0;
 
 // Wait limit (>= 0; 0 = kTimeoutNs) and the stall test hook: off, or a
 // role of 1 or 2 with an idle time of at most one second.
@@ -316,7 +325,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (st != FD_OK) return st;
     fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0};
     if (options) opt = *options;
-    if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 ||
+    if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 || opt.ctas_per_sm > 8 ||
         opt.split_margin_pct < 0 || opt.split_margin_pct > 100 ||
         (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128 && opt.tile_tokens != 256) ||
         !hooks_valid(opt.timeout_us, opt.debug_stall_us, opt.debug_stall_role))
@@ -368,7 +377,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         long long items = 0;
     };
     auto make_shape = [&](int tile_opt, int cps, Shape &sh) -> bool {
-        sh.ks = kernel_shape(p, tile_opt, fold);
+        sh.ks = kernel_shape(p, tile_opt, fold, cps);
         sh.cps = cps;
         const int tile = sh.ks.tile;
         const int qrows = 8 * sh.ks.nt;
@@ -411,7 +420,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     const int cps_opt = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
     int tile_opt = opt.tile_tokens;
     if (tile_opt == 0 && p.kv_dtype == FD_E4M3) {
-        const KernelShape k256 = kernel_shape(p, 256, fold);
+        const KernelShape k256 = kernel_shape(p, 256, fold, cps_opt);
         if (k256.tile == 256 && (long long)decode_smem_bytes(p, k256, 3) <= smem_limit(cps_opt)) tile_opt = 256;
     }
     Shape sh;
@@ -425,9 +434,15 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         long long tok = 0;
         for (int L : lens) tok += L;
         const double mean_item = (double)tok * p.Hkv * sh.nhg / (double)sh.items;
-        const bool shallow = sh.stages < 3 || (p.kv_dtype == FD_E4M3 && sh.ks.tile < 256);
+        double limit;
+        if (p.kv_dtype == FD_E4M3)
+            limit = sh.ks.tile < 256 ? INFINITY : kShortItemTokensE4m3;
+        else
+            limit = sh.stages < 3 ? kShortItemTokensShallow : kShortItemTokens;
+        // E4M3: 128-token stages of 4 warps x 2 sub-tiles; 16-bit: 64-token stages.
+        const int tile2 = p.kv_dtype == FD_E4M3 ? 128 : 64;
         Shape s2;
-        if (mean_item < (shallow ? kShortItemTokensShallow : kShortItemTokens) && make_shape(64, 2, s2)) {
+        if (mean_item < limit && make_shape(tile2, 2, s2)) {
             bool fits = s2.ks.nt == 1 || p.D == 64;  // register budget of two 5-warp CTAs
             if (have_dev) {
                 int blocks = 0;
@@ -462,6 +477,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     plan->kv_rows = kv_rows;
     plan->row_fold = fold;
     plan->head_subgroups = nhg;
+    plan->ctas_per_sm = sh.cps;
     plan->timeout_us = opt.timeout_us;
     plan->debug_stall_us = opt.debug_stall_us;
     plan->debug_stall_role = opt.debug_stall_role;
@@ -500,7 +516,8 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     const int fold = plan->row_fold;
     if (fold < 1 || plan->kv_rows < 1 || plan->kv_rows * fold != p.B || plan->head_subgroups < 1) return FD_ERR_INVALID_ARG;
     if (fold > 1 && ex && (ex->cache_batch_idx || ex->cache_leftpad)) return FD_ERR_UNSUPPORTED;
-    const KernelShape ks = kernel_shape(p, plan->tile_tokens, fold);
+    if (plan->ctas_per_sm < 0 || plan->ctas_per_sm > 8) return FD_ERR_INVALID_ARG;
+    const KernelShape ks = kernel_shape(p, plan->tile_tokens, fold, std::max(1, plan->ctas_per_sm));
     if (plan->head_subgroups != ((p.Hq / p.Hkv) * fold + 8 * ks.nt - 1) / (8 * ks.nt)) return FD_ERR_INVALID_ARG;
     if (plan->tile_tokens != ks.tile || plan->chunk_tokens < ks.tile || plan->chunk_tokens % ks.tile != 0 ||
         plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->stages < kMinStages ||

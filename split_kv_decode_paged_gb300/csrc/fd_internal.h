@@ -97,9 +97,11 @@ struct KernelShape {
     int nt;              // 8-wide head tiles: 1 (G <= 8) or 2 (G <= 16)
 };
 
-// tile_tokens: 64 or 128 (0 = default for the K/V type); fold: q sequences
-// per KV row (1 = ordinary decode).
-KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold);
+// tile_tokens: 64, 128 or 256 (0 = default for the K/V type); fold: q
+// sequences per KV row (1 = ordinary decode); ctas_per_sm: persistent CTAs
+// per SM (E4M3 128-token stages with two or more CTAs per SM take 4 consumer
+// warps x 2 sub-tiles, which fit two to an SM).
+KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold, int ctas_per_sm);
 size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages);
 int decode_max_stages(const fd_problem &p, const KernelShape &ks);
 // Resident CTAs per SM of the decode kernel of this shape with smem bytes of

@@ -231,8 +231,9 @@ def test_many_splits_up_to_the_maximum(fdlib, L, splits, want, fuse):
 @pytest.mark.parametrize("kv,q,ps,D", [("bf16", "bf16", 16, 128), ("e4m3", "bf16", 128, 128), ("f16", "f16", 32, 64),
                                        ("e4m3", "f16", 64, 128)])
 def test_short_items_two_ctas_per_sm(fdlib, kv, q, ps, D):
-    """Many short sequences: the planner runs two CTAs per SM with 64-token
-    stages (4 consumer warps); every row against the oracle, with empty,
+    """Many short sequences: the planner runs two CTAs per SM with 4 consumer
+    warps each (64-token stages for 16-bit K/V, 128-token stages of two
+    sub-tiles per warp for E4M3); every row against the oracle, with empty,
     one-token and page-boundary lengths among them."""
     rng = np.random.default_rng(31 + ps)
     B = 700
@@ -243,4 +244,16 @@ def test_short_items_two_ctas_per_sm(fdlib, kv, q, ps, D):
     spec = _spec(f"short {kv}", B, 32, 8, D, ps, kv, q, lens.tolist())
     err, dec = _run_and_check(spec, 17 + ps)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert dec.plan.tile_tokens == 64 and dec.plan.grid_ctas == 2 * sms
+    assert dec.plan.ctas_per_sm == 2 and dec.plan.grid_ctas == 2 * sms
+    assert dec.plan.tile_tokens == (128 if kv == "e4m3" else 64)
+
+
+@pytest.mark.parametrize("Hq,D,splits,fuse", [(16, 128, 0, 1), (16, 128, 3, 1), (32, 64, 2, 0), (32, 64, 4, 1)])
+def test_fp8_two_ctas_128_token_stages(fdlib, Hq, D, splits, fuse):
+    """E4M3 pools with two CTAs per SM and 128-token stages of 4 warps x 2
+    sub-tiles (the short-item shape), forced: G = 8 and, at D = 64, G = 16
+    (two head tiles); split with the fused and the separate merge."""
+    lens = [0, 1, 127, 128, 129, 700, 3000, 255, 256, 64]
+    spec = _spec(f"fp8 4x2 G={Hq // 2} D={D}", len(lens), Hq, 2, D, 64, "e4m3", "bf16", lens)
+    err, dec = _run_and_check(spec, 41 + D + splits, num_splits=splits, fuse_merge=fuse, tile_tokens=128, ctas_per_sm=2)
+    assert dec.plan.tile_tokens == 128 and dec.plan.ctas_per_sm == 2

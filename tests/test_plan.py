@@ -133,21 +133,26 @@ SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per 
     (torch.bfloat16, 16, 2048, 1024, True),    # ... unless the default lost a stage to its tables
     (torch.bfloat16, 16, 2048, 2048, False),
     (torch.float8_e4m3fn, 128, 512, 512, True),
-    (torch.float8_e4m3fn, 128, 512, 1024, False),
-    (torch.float8_e4m3fn, 128, 2048, 1024, True),
+    (torch.float8_e4m3fn, 128, 512, 1536, True),
+    (torch.float8_e4m3fn, 128, 512, 3072, False),  # 256-token stages win on long items
+    (torch.float8_e4m3fn, 128, 2048, 2048, True),   # ... unless the tables took them away
+    (torch.float8_e4m3fn, 16, 512, 3072, True),     # 16-token pages: always two CTAs
     (torch.bfloat16, 16, 16, 256, False),      # 128 items cannot fill two CTAs on every SM
 ])
 def test_short_items_take_two_ctas_per_sm(kv, ps, B, L, want_two):
-    """The planner's shape for many short work items: 64-token stages with two
-    persistent CTAs per SM (one streams while the other is between items)."""
+    """The planner's shape for many short work items: two persistent CTAs per
+    SM (one streams while the other is between items)."""
     nb = 4096 // ps
+    assert L <= nb * ps
     prob = _lib.make_problem(B, 32, 8, 128, ps, nb, B * nb, torch.bfloat16, kv)
     plan = _lib.fd_plan(prob, [L] * B, num_sms=152)
     if want_two:
-        assert plan.tile_tokens == 64 and plan.grid_ctas == 2 * 152 and plan.stages >= 2
-        assert plan.smem_bytes <= (SM_SMEM - 2 * RESERVED) // 2
+        # 16-bit K/V: 64-token stages (4 warps); E4M3: 128-token stages (4 warps x 2 sub-tiles)
+        want_tile = 128 if kv == torch.float8_e4m3fn else 64
+        assert plan.tile_tokens == want_tile and plan.ctas_per_sm == 2 and plan.grid_ctas == 2 * 152
+        assert plan.stages >= 2 and plan.smem_bytes <= (SM_SMEM - 2 * RESERVED) // 2
     else:
-        assert plan.tile_tokens >= 128 and plan.grid_ctas <= 152
+        assert plan.ctas_per_sm == 1 and plan.grid_ctas <= 152 and plan.tile_tokens >= 128
 
 
 def test_short_items_rule_respects_explicit_options_and_registers(fdlib):
