@@ -529,9 +529,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                     lens[b] = L;
                 }
             }
+            auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
+            if (B == 1) {
+                // One KV row (a single long request): its full chunks, then
+                // its partial chunk; no ordering to build.
+                __syncwarp();
+                const int L = lens[0];
+                totalA = (L / C) * HG;
+                nB = tail_of(L) >= 0 ? 1 : 0;
+                if (lane == 0) {
+                    bpre[0] = 0;
+                    bpre[1] = totalA;
+                    order[0] = 0;
+                }
+                __syncwarp();
+            } else {
             for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
             __syncwarp();
-            auto tail_of = [&](int L) { return (L == 0 || L % C) ? L % C : -1; };  // -1: no partial chunk
             // Bucket of a partial chunk of r < C tokens: r >> bsh < 64 for all of
             // them (buckets 2^bsh tokens wide, C / 64 < 2^bsh <= C / 32), longer
             // chunks in lower buckets.  A shift, not a division: this runs once
@@ -588,6 +602,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 __syncwarp();
             }
             totalA = runningA;
+            }
         }
         const int total = totalA + nB * HG;
 
