@@ -359,6 +359,77 @@ int orc_decode_paged_ex(const orc_problem *p, int cache_rows, const int32_t *cac
     return ORC_OK;
 }
 
+/* Query token i of q_len (causal, aligned to the end of the cache): its
+ * scores over the tokens it may see, their maximum, the exponentials, the
+ * weighted sum of V and its normalisation -- the definition, written out for
+ * one (b, i, hq) with the query row given explicitly. */
+static int attend_causal(const orc_inputs *in, int b, int hq, const double *qrow, int t_end, double *out,
+                         double *lse) {
+    const orc_problem *p = in->p;
+    const int D = p->D, kvh = hq / (p->Hq / p->Hkv);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (t_end <= 0) {
+        *lse = -INFINITY;
+        return ORC_OK;
+    }
+    double *s = (double *)malloc(sizeof(double) * (size_t)t_end);
+    double *row = (double *)malloc(sizeof(double) * (size_t)D);
+    int rc = (s && row) ? ORC_OK : ORC_ERR_NOMEM;
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    for (int t = 0; t < t_end && rc == ORC_OK; ++t) {
+        rc = row_of(in, 0, b, kvh, t, row);
+        if (rc) break;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qrow[d] * row[d];
+        s[t] = dot * inv_sqrt_d;
+    }
+    if (rc == ORC_OK) {
+        double mx = -INFINITY;
+        for (int t = 0; t < t_end; ++t) if (s[t] > mx) mx = s[t];
+        double z = 0.0;
+        for (int t = 0; t < t_end && rc == ORC_OK; ++t) {
+            const double w = exp(s[t] - mx);
+            z += w;
+            rc = row_of(in, 1, b, kvh, t, row);
+            if (rc) break;
+            for (int d = 0; d < D; ++d) out[d] += w * row[d];
+        }
+        if (rc == ORC_OK) {
+            for (int d = 0; d < D; ++d) out[d] /= z;
+            *lse = mx + log(z);
+        }
+    }
+    free(s);
+    free(row);
+    return rc;
+}
+
+int orc_decode_paged_multi(const orc_problem *p, int q_len, const void *q, const void *k_pages,
+                           const void *v_pages, const float *k_scale, const float *v_scale,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           double *out, double *lse) {
+    if (check_problem(p) || q_len < 1) return ORC_ERR_ARG;
+    if (p->kv_dtype == ORC_E4M3 && (!k_scale || !v_scale)) return ORC_ERR_ARG;
+    const int D = p->D;
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!qrow) return ORC_ERR_NOMEM;
+    orc_inputs in = {p, NULL, k_pages, v_pages, k_scale, v_scale, block_table, NULL, NULL, 0};
+    int rc = ORC_OK;
+    for (int b = 0; b < p->B && rc == ORC_OK; ++b) {
+        const int L = seq_lens[b];
+        if (L < q_len) { rc = ORC_ERR_ARG; break; }
+        for (int i = 0; i < q_len && rc == ORC_OK; ++i) {
+            for (int hq = 0; hq < p->Hq && rc == ORC_OK; ++hq) {
+                const size_t r = ((size_t)b * q_len + i) * p->Hq + hq;  /* [B, q_len, Hq] */
+                for (int d = 0; d < D; ++d) qrow[d] = load_elem(q, p->q_dtype, r * D + d);
+                rc = attend_causal(&in, b, hq, qrow, L - q_len + i + 1, out + r * D, lse + r);
+            }
+        }
+    }
+    free(qrow);
+    return rc;
+}
+
 int orc_decode_contiguous(const orc_problem *p, int max_seqlen, const void *q,
                           const void *k_cache, const void *v_cache,
                           const int32_t *seq_lens, double *out, double *lse) {

@@ -88,6 +88,19 @@ int orc_decode_paged_pairs(const orc_problem *p, const void *q, const void *k_pa
  * [leftpad[cb], seq_lens[cb]) (leftpad 0 when NULL).  cache_rows = rows of
  * block_table / seq_lens / leftpad.  Returns ORC_ERR_ARG for an index outside
  * the cache or a leftpad outside [0, seq_len]. */
+/* Several query tokens per sequence, causal among them ("Inference Cookbook"
+ * §3.2-3.3: flash_attn_with_kvcache with seqlen_q >= 1 and causal=True after
+ * the new tokens' K/V were written into the cache; "FlashDecoding 与
+ * FlashInfer 深度解析" §3.1, the append mode).  q [B, q_len, Hq, D]: query
+ * token i of sequence b is the i-th of its last q_len cached tokens and
+ * attends the tokens [0, L_b - q_len + i + 1) (the causal mask aligned to the
+ * end of the cache).  out [B, q_len, Hq, D], lse [B, q_len, Hq].  Requires
+ * L_b >= q_len. */
+int orc_decode_paged_multi(const orc_problem *p, int q_len, const void *q, const void *k_pages,
+                           const void *v_pages, const float *k_scale, const float *v_scale,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           double *out, double *lse);
+
 int orc_decode_paged_ex(const orc_problem *p, int cache_rows, const int32_t *cache_batch_idx,
                         const int32_t *cache_leftpad, const void *q, const void *k_pages,
                         const void *v_pages, const float *k_scale, const float *v_scale,

@@ -53,6 +53,8 @@ def lib():
         L.orc_rotary_f32.argtypes = [P, I, I, I, P, P, I, P]
         L.orc_append_kv_rotary.restype = I
         L.orc_append_kv_rotary.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P, P, P, P, P, I, I, I, P]
+        L.orc_decode_paged_multi.restype = I
+        L.orc_decode_paged_multi.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P, P, P, P]
         L.orc_decode_contiguous.restype = I
         L.orc_decode_contiguous.argtypes = [ctypes.POINTER(Problem), I, P, P, P, P, P, P]
         L.orc_partial_state.restype = I
@@ -157,6 +159,20 @@ def decode_paged_ex(p, cache_rows, cache_batch_idx, cache_leftpad, q, k_pages, v
     rc = lib().orc_decode_paged_ex(ctypes.byref(p), int(cache_rows), _ptr(bi), _ptr(lp), _ptr(q), _ptr(k), _ptr(v),
                                    _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl), _ptr(out), _ptr(lse))
     _check(rc, "decode_paged_ex")
+    return out, lse
+
+
+def decode_paged_multi(p, q_len, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens):
+    """q_len causal query tokens per sequence: q [B, q_len, Hq, D] ->
+    (out [B, q_len, Hq, D] f64, lse [B, q_len, Hq] f64)."""
+    q, k, v = raw(q), raw(k_pages), raw(v_pages)
+    ks, vs = raw(k_scale), raw(v_scale)
+    bt, sl = raw(block_table).astype(np.int32), raw(seq_lens).astype(np.int32)
+    out = np.zeros((p.B, q_len, p.Hq, p.D), np.float64)
+    lse = np.zeros((p.B, q_len, p.Hq), np.float64)
+    rc = lib().orc_decode_paged_multi(ctypes.byref(p), int(q_len), _ptr(q), _ptr(k), _ptr(v), _ptr(ks), _ptr(vs),
+                                      _ptr(bt), _ptr(sl), _ptr(out), _ptr(lse))
+    _check(rc, "decode_paged_multi")
     return out, lse
 
 
