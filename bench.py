@@ -545,6 +545,76 @@ def bench_ex(args):
         "gpu_launches_per_call": 1}))
 
 
+def bench_multi(args):
+    """Several query tokens per sequence (causal among them) on the GQA batch:
+    q [64, 4, 32, 128], token i of 4 attending the cached tokens
+    [0, L - 4 + i + 1), in one call that streams each sequence's K/V once,
+    against four one-token decodes of the same tokens (each over its own
+    prefix), both back to back."""
+    from split_kv_decode_paged_gb300 import workloads as W
+    import split_kv_decode_paged_gb300 as fd
+    from split_kv_decode_paged_gb300 import build as fd_build
+    fd_build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q_len = 4
+    wl = W.make_config(3, dev)
+    spec = wl.spec
+    B, Hq, D = spec.B, spec.Hq, spec.D
+    g = torch.Generator(device=dev).manual_seed(404)
+    qm = torch.randn((B, q_len, Hq, D), generator=g, device=dev).to(wl.q.dtype)
+    dec = fd.PagedDecoder.for_pools(qm, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens.cpu())
+    out = torch.empty_like(qm)
+    lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=dev)
+    singles = []
+    for i in range(q_len):
+        lens_i = (wl.seq_lens - (q_len - 1 - i)).to(torch.int32)
+        d1 = fd.PagedDecoder.for_pools(wl.q, wl.k_pages, wl.v_pages, wl.block_table, lens_i.cpu())
+        singles.append((d1, qm[:, i].contiguous(), lens_i, torch.empty_like(wl.q),
+                        torch.empty((B, Hq), dtype=torch.float32, device=dev)))
+
+    def run_multi():
+        dec(qm, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens, out=out, lse=lse)
+
+    def run_singles():
+        for d1, qi, li, oi, si in singles:
+            d1(qi, wl.k_pages, wl.v_pages, wl.block_table, li, out=oi, lse=si)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("fd_timed")
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        return a.elapsed_time(b) * 1e3 / args.steps
+
+    us_multi, us_singles = timed(run_multi), timed(run_singles)
+    dec.check()
+    for d1, *_ in singles:
+        d1.check()
+    lens = wl.seq_lens.cpu()
+    nbytes = W.algorithmic_bytes(spec, lens) + (q_len - 1) * B * Hq * (D * 4 + 4)  # + 3 more q/out rows and lse
+    peak, kind = measured_peak()
+    plan = dec.plan
+    print(json.dumps({
+        "metric": "multi-token decode achieved HBM GB/s", "value": nbytes / us_multi / 1e3, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "us_per_call": us_multi,
+        "four_single_token_decodes_us": us_singles, "speedup_vs_single_token_decodes": us_singles / us_multi,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "bytes": nbytes,
+        "frac_of_peak": nbytes / us_multi / 1e3 / peak, "peak": peak, "peak_source": kind,
+        "plan": {"q_len": plan.q_len, "num_splits": plan.num_splits, "head_subgroups": plan.head_subgroups,
+                 "tile_tokens": plan.tile_tokens, "ctas_per_sm": plan.ctas_per_sm},
+        "config": {"workload": "GQA batch (B=64, Hq=32, Hkv=8, D=128, bf16, 16-token pages, lengths U[512, 8192], "
+                               "seed 1003) with 4 causal query tokens per sequence (q seed 404)",
+                   "l2": "inputs > 2x L2: back to back, one event pair"},
+        "gpu_launches_per_call": 1}))
+
+
 def bench_large(args):
     """The plain decode on two large batches (1024 bf16 sequences of 256-1024
     tokens; 2048 FP8 sequences of 16-4096 tokens), timed back to back like the
@@ -703,10 +773,12 @@ def main():
     ap.add_argument("--per-config-cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", default="decode", choices=["decode", "cascade", "append", "merge", "ex", "large"],
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "cascade", "append", "merge", "ex", "large", "multi"],
                     help="cascade: shared-prefix batch, cascade vs plain decode; append: fd_append_kv (plain "
                          "and rotary); merge: fd_merge_states; ex: fd_decode_paged_ex with cache_batch_idx "
-                         "and left padding")
+                         "and left padding; large: two large batches; multi: 4 causal query tokens per "
+                         "sequence on the GQA batch")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed decode calls (no warm-L2/graph/e2e extras, no CPU baseline)")
     args = ap.parse_args()
@@ -718,7 +790,7 @@ def main():
                               "unavailable": f"the {args.workload} workload is measured on the GPU path only"}))
             return
         {"cascade": bench_cascade, "append": bench_append, "merge": bench_merge, "ex": bench_ex,
-         "large": bench_large}[args.workload](args)
+         "large": bench_large, "multi": bench_multi}[args.workload](args)
         return
     from split_kv_decode_paged_gb300 import workloads as W
     ws, rank, local = dist_env()

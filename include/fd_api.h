@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define FD_API_VERSION 2
+#define FD_API_VERSION 3
 
 typedef enum {
     FD_OK = 0,
@@ -120,6 +120,17 @@ typedef struct {
                            than timeout_us, it makes the other side's waits
                            run out, exercising the timeout path.  <= 1 s.   */
     int debug_stall_role; /* 0, 1 (producer) or 2 (consumers)                */
+    int q_len;          /* query tokens per sequence, 0 or 1 = one (decode).
+                           q_len > 1 (at most 64): the last q_len cached tokens
+                           of every sequence are its queries and token i of
+                           them attends the cached tokens
+                           [0, seq_lens[b] - q_len + i + 1) -- causal attention
+                           aligned to the end of the cache, after the new
+                           tokens' K/V were appended ("Inference Cookbook"
+                           §3.2-3.3, causal=True; [P1] §3.1, the append mode).
+                           q and out are [B, q_len, Hq, D], lse [B, q_len, Hq];
+                           problem->B counts sequences; not with shared_kv or
+                           the fd_decode_extras indirections               */
 } fd_plan_options;
 
 /* A plan: plain data in host memory, owned by the caller, reusable for any
@@ -147,7 +158,9 @@ typedef struct {
     int timeout_us;       /* device wait limit (0 = 2 s), from the options       */
     int debug_stall_us;   /* test hook copied from the options (0 = off)         */
     int debug_stall_role;
-    int reserved[1];
+    int q_len;            /* query tokens per sequence (1 = decode); problem.B
+                             then counts query rows, B * q_len               */
+    int reserved[3];
 } fd_plan_t;
 
 /* Plan a decode call [P1 §2.1 step 1; P2 进阶突破; P3 §6.3, §8.2].
@@ -168,6 +181,9 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host,
 
 /* One decode step [P1 §2.1; P2 stages one and two; P3 §3.5, §4, §6, §7].
  *   q, k_pages, v_pages  device, 16-byte aligned, layouts as in fd_problem
+ *                        (with plan->q_len > 1: q and out [B, q_len, Hq, D],
+ *                        lse [B, q_len, Hq], the q_len causal query tokens of
+ *                        each sequence; see fd_plan_options.q_len)
  *   k_scale, v_scale     device fp32 [num_pages, Hkv] for FD_E4M3 (value =
  *                        e4m3 code * scale); must be NULL otherwise
  *   block_table, seq_lens device int32; the call attends over tokens

@@ -36,7 +36,13 @@ class PagedDecoder:
 
     @classmethod
     def for_pools(cls, q, k_pages, v_pages, block_table, seq_lens_host, out_dtype=None, **plan_opts):
-        B, Hq, D = q.shape
+        """q [B, Hq, D], or [B, q_len, Hq, D] for q_len causal query tokens
+        per sequence (the last q_len cached tokens of each)."""
+        if q.dim() == 4:
+            B, q_len, Hq, D = q.shape
+            plan_opts.setdefault("q_len", q_len)
+        else:
+            B, Hq, D = q.shape
         num_pages, page_size, Hkv, D2 = k_pages.shape
         if D2 != D:
             raise ValueError("head dimension of q and the pools differ")
@@ -46,11 +52,12 @@ class PagedDecoder:
 
     def __call__(self, q, k_pages, v_pages, block_table, seq_lens, k_scale=None, v_scale=None, out=None,
                  lse=None, want_lse=True, stream=None):
-        p = self.problem
+        p, plan = self.problem, self.plan
+        lead = (p.B,) if plan.q_len <= 1 else (p.B, plan.q_len)  # p: the caller's problem (B sequences)
         if out is None:
-            out = torch.empty((p.B, p.Hq, p.D), dtype=_lib.FD_TO_TORCH[p.out_dtype], device=q.device)
+            out = torch.empty(lead + (p.Hq, p.D), dtype=_lib.FD_TO_TORCH[p.out_dtype], device=q.device)
         if lse is None and want_lse:
-            lse = torch.empty((p.B, p.Hq), dtype=torch.float32, device=q.device)
+            lse = torch.empty(lead + (p.Hq,), dtype=torch.float32, device=q.device)
         fd_decode_paged(self.plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse,
                         self.workspace, self.status, stream)
         return out, lse
@@ -107,7 +114,7 @@ class HostStep:
     holding out and lse (typed views of both), and their device twins."""
 
     def __init__(self, dec: PagedDecoder):
-        p, plan = dec.problem, dec.plan
+        p, plan = dec.plan.problem, dec.plan  # p.B counts query rows (B * q_len)
         lay = _lib.fd_host_io_layout_for(plan)
         self.layout = lay
         self.host_in = torch.empty(lay.in_bytes, dtype=torch.uint8).pin_memory()
@@ -121,9 +128,10 @@ class HostStep:
             nb = n * torch.empty((), dtype=dtype).element_size()
             return buf[off:off + nb].view(dtype).view(shape)
 
-        self.q = view(self.host_in, lay.q_offset, p.B * p.Hq * p.D, qt, (p.B, p.Hq, p.D))
+        lead = (p.B,) if plan.q_len <= 1 else (kv_rows, plan.q_len)
+        self.q = view(self.host_in, lay.q_offset, p.B * p.Hq * p.D, qt, lead + (p.Hq, p.D))
         self.block_table = view(self.host_in, lay.block_table_offset, kv_rows * p.max_blocks_per_seq, torch.int32,
                                 (kv_rows, p.max_blocks_per_seq))
         self.seq_lens = view(self.host_in, lay.seq_lens_offset, kv_rows, torch.int32, (kv_rows,))
-        self.out = view(self.host_out, lay.out_offset, p.B * p.Hq * p.D, ot, (p.B, p.Hq, p.D))
-        self.lse = view(self.host_out, lay.lse_offset, p.B * p.Hq, torch.float32, (p.B, p.Hq))
+        self.out = view(self.host_out, lay.out_offset, p.B * p.Hq * p.D, ot, lead + (p.Hq, p.D))
+        self.lse = view(self.host_out, lay.lse_offset, p.B * p.Hq, torch.float32, lead + (p.Hq,))

@@ -49,7 +49,7 @@ class FdPlanOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("num_sms", ctypes.c_int), ("fuse_merge", ctypes.c_int),
                 ("max_seq_len", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("split_margin_pct", ctypes.c_int),
                 ("tile_tokens", ctypes.c_int), ("shared_kv", ctypes.c_int), ("timeout_us", ctypes.c_int),
-                ("debug_stall_us", ctypes.c_int), ("debug_stall_role", ctypes.c_int)]
+                ("debug_stall_us", ctypes.c_int), ("debug_stall_role", ctypes.c_int), ("q_len", ctypes.c_int)]
 
 
 class FdDecodeExtras(ctypes.Structure):
@@ -66,7 +66,7 @@ class FdPlan(ctypes.Structure):
                 ("ws_counters", ctypes.c_size_t), ("work_items_hint", ctypes.c_longlong),
                 ("kv_rows", ctypes.c_int), ("row_fold", ctypes.c_int), ("head_subgroups", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("timeout_us", ctypes.c_int), ("debug_stall_us", ctypes.c_int),
-                ("debug_stall_role", ctypes.c_int), ("reserved", ctypes.c_int * 1)]
+                ("debug_stall_role", ctypes.c_int), ("q_len", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n not in ("problem", "reserved")}
@@ -183,6 +183,16 @@ class _Args:
                 self._fail(name, f"is on {t.device}, other arguments on {device}")
 
 
+def _rows_shape(plan, t, tail):
+    """Query-row tensors are [rows, *tail]; with several query tokens per
+    sequence also [B, q_len, *tail] (the same memory)."""
+    p = plan.problem
+    flat = (p.B,) + tail
+    if t is not None and t.dim() == len(tail) + 2 and plan.row_fold == max(1, plan.q_len):
+        return (plan.kv_rows, max(1, plan.q_len)) + tail
+    return flat
+
+
 def _check_decode(entry, plan, q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, out, lse, workspace,
                   status, table_rows=None, host_io=False):
     p = plan.problem
@@ -191,11 +201,11 @@ def _check_decode(entry, plan, q, k_pages, v_pages, k_scale, v_scale, block_tabl
     pool = (p.num_pages, p.page_size, p.Hkv, p.D)
     rows = table_rows if table_rows is not None else (plan.kv_rows if plan.kv_rows > 0 else p.B)
     if not host_io:
-        a.tensor("q", q, FD_TO_TORCH[p.q_dtype], (p.B, p.Hq, p.D))
+        a.tensor("q", q, FD_TO_TORCH[p.q_dtype], _rows_shape(plan, q, (p.Hq, p.D)))
         a.tensor("block_table", block_table, torch.int32, (rows, p.max_blocks_per_seq))
         a.tensor("seq_lens", seq_lens, torch.int32, (rows,))
-        a.tensor("out", out, FD_TO_TORCH[p.out_dtype], (p.B, p.Hq, p.D))
-        a.tensor("lse", lse, torch.float32, (p.B, p.Hq), optional=True)
+        a.tensor("out", out, FD_TO_TORCH[p.out_dtype], _rows_shape(plan, out, (p.Hq, p.D)))
+        a.tensor("lse", lse, torch.float32, _rows_shape(plan, lse, (p.Hq,)), optional=True)
     a.tensor("k_pages", k_pages, kv, pool)
     a.tensor("v_pages", v_pages, kv, pool)
     if p.kv_dtype == FD_E4M3:
@@ -229,16 +239,17 @@ def make_problem(B, Hq, Hkv, D, page_size, max_blocks_per_seq, num_pages, q_dtyp
 
 def fd_plan(problem: FdProblem, seq_lens_host, num_splits=0, num_sms=0, fuse_merge=1, max_seq_len=0,
             ctas_per_sm=0, split_margin_pct=0, tile_tokens=0, shared_kv=0, timeout_us=0, debug_stall_us=0,
-            debug_stall_role=0) -> FdPlan:
+            debug_stall_role=0, q_len=0) -> FdPlan:
     """Plan a decode call; seq_lens_host is a host int32 tensor/sequence.
     timeout_us bounds every device-side wait (0 = 2 s); debug_stall_us and
-    debug_stall_role are the test hook of the timeout path (0 = off)."""
+    debug_stall_role are the test hook of the timeout path (0 = off); q_len
+    > 1 plans q_len causal query tokens per sequence (q [B, q_len, Hq, D])."""
     lens = torch.as_tensor(seq_lens_host, dtype=torch.int32).cpu().contiguous()
     if lens.numel() != problem.B and not (shared_kv and lens.numel() >= 1):
         raise ValueError("seq_lens_host must have B entries")
     opts = FdPlanOptions(int(num_splits), int(num_sms), int(fuse_merge), int(max_seq_len), int(ctas_per_sm),
                          int(split_margin_pct), int(tile_tokens), int(shared_kv), int(timeout_us),
-                         int(debug_stall_us), int(debug_stall_role))
+                         int(debug_stall_us), int(debug_stall_role), int(q_len))
     plan = FdPlan()
     rc = load().fd_plan(ctypes.byref(problem), ctypes.c_void_p(lens.data_ptr()), ctypes.byref(opts),
                         ctypes.byref(plan))

@@ -11,6 +11,12 @@ namespace fd {
 template <int KV, int D, int NT, bool QBF16>
 cudaError_t launch_decode_d(const KernelShape &ks, const DecodeParams &dp, const CUtensorMap &tmk,
                             const CUtensorMap &tmv, int grid, size_t smem, cudaStream_t stream) {
+    if (dp.qn > 1) {
+        // several causal query tokens per KV row: the 128-token, 8-warp shape only
+        if (ks.consumer_warps == 8 && ks.subtiles == 1)
+            return launch_decode_t<KV, D, NT, 8, 1, QBF16, true>(dp, tmk, tmv, grid, smem, stream);
+        return cudaErrorInvalidValue;
+    }
     if (ks.consumer_warps == 4 && ks.subtiles == 1)
         return launch_decode_t<KV, D, NT, 4, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);
     if constexpr (KV == KV_E4M3) {

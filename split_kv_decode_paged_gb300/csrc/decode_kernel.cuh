@@ -61,6 +61,9 @@ struct StageMeta {
     float kscale[kMaxBoxesPerTile];
     float vscale[kMaxBoxesPerTile];
 };
+// The stage barriers (8-byte mbarriers) follow the array of StageMeta in
+// shared memory.
+static_assert(sizeof(StageMeta) % 8 == 0, "StageMeta keeps the barriers after it 8-byte aligned");
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -402,7 +405,10 @@ __device__ __noinline__ void build_dispatch_tables_coop(const DecodeParams &p, i
     __syncthreads();
 }
 
-template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
+// CAUSAL: several query tokens per KV row (DecodeParams::qn > 1), each with
+// its own causal limit; a separate instance so the one-token decode carries
+// none of it.
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16, bool CAUSAL>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     fd_split_kv_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmv) {
@@ -422,15 +428,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     float *scr_lse = scr_inv + QROWS;      // per head: combined max (log2 units)
     int *scr_flag = reinterpret_cast<int *>(scr_lse + QROWS);
     StageMeta *meta = reinterpret_cast<StageMeta *>(reinterpret_cast<uint8_t *>(scratch) + align_up(Sh::SCRATCH, 128));
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(meta + NST);
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(meta + NST) + 7) & ~uintptr_t(7));
     uint64_t *empty_bar = full_bar + NST;
-    // Dispatch tables (sized for p.B >= the KV rows): item prefix at 32-row
-    // block boundaries, attended length per row, partial-chunk row order.
-    const int nblk = (p.B + 31) / 32;
+    // Dispatch tables of the KV rows: item prefix at 32-row block
+    // boundaries, attended length per row, partial-chunk row order.
+    const int nblk = (p.Bkv + 31) / 32;
     int *bpre = reinterpret_cast<int *>(empty_bar + NST);  // nblk + 1
-    int *lens = bpre + nblk + 1;                           // B
-    int *hist = lens + p.B;                                // kOrderBuckets
-    uint16_t *order = reinterpret_cast<uint16_t *>(hist + kOrderBuckets);  // B
+    int *lens = bpre + nblk + 1;                           // Bkv
+    int *hist = lens + p.Bkv;                              // kOrderBuckets
+    uint16_t *order = reinterpret_cast<uint16_t *>(hist + kOrderBuckets);  // Bkv
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -649,6 +655,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             it.hg = r2 - it.kvh * NHG;
             it.nrows = min(QROWS, p.G * p.fold - it.hg * QROWS);
             it.L = lens[it.b];
+            // several query tokens per row need at least that many cached tokens
+            if constexpr (CAUSAL)
+                if (it.L < p.qn && lane == 0) flag_status(p.status, FD_DEV_CAPACITY);
             it.nsplit = it.L == 0 ? 1 : (it.L + C - 1) / C;
             it.cb = it.b;
             int lp = 0;
@@ -1039,10 +1048,26 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                         sc0 *= qd[n][0];
                         sc1 *= qd[n][1];
                     }
-                    sv[sub][n][0] = v0 ? (sv[sub][n][0] + s2[n][0]) * sc0 : -INFINITY;
-                    sv[sub][n][1] = v0 ? (sv[sub][n][1] + s2[n][1]) * sc1 : -INFINITY;
-                    sv[sub][n][2] = v1 ? (sv[sub][n][2] + s2[n][2]) * sc0 : -INFINITY;
-                    sv[sub][n][3] = v1 ? (sv[sub][n][3] + s2[n][3]) * sc1 : -INFINITY;
+                    bool v00 = v0, v01 = v0, v10 = v1, v11 = v1;
+                    if constexpr (CAUSAL) {
+                        // causal: q row i of the item is query token i / G of
+                        // the KV row and sees the cached tokens
+                        // [0, L - qn + i / G + 1); token t of the tile row is
+                        // hidden from the score columns (q rows 2c, 2c + 1 of
+                        // head tile n) whose limit it reaches
+                        const int ta = mt.t0 + r0 + g;
+                        const int i0 = mt.hg * QROWS + n * 8 + 2 * c;
+                        const int L = lens[mt.b];  // the row's attended length (dispatch table)
+                        const int l0 = L - p.qn + i0 / p.G + 1, l1 = L - p.qn + (i0 + 1) / p.G + 1;
+                        v00 = v00 && ta < l0;
+                        v01 = v01 && ta < l1;
+                        v10 = v10 && ta + 8 < l0;
+                        v11 = v11 && ta + 8 < l1;
+                    }
+                    sv[sub][n][0] = v00 ? (sv[sub][n][0] + s2[n][0]) * sc0 : -INFINITY;
+                    sv[sub][n][1] = v01 ? (sv[sub][n][1] + s2[n][1]) * sc1 : -INFINITY;
+                    sv[sub][n][2] = v10 ? (sv[sub][n][2] + s2[n][2]) * sc0 : -INFINITY;
+                    sv[sub][n][3] = v11 ? (sv[sub][n][3] + s2[n][3]) * sc1 : -INFINITY;
                 }
             }
 
@@ -1386,16 +1411,16 @@ size_t decode_smem_for(int stages, int B) {
 // memory (registers, threads and shared memory all counted).
 template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
 cudaError_t occupancy_t(size_t smem, int *blocks) {
-    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16>;
+    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, kern, DecodeShape<KV, D, NT, NC, SUBT>::THREADS, smem);
 }
 
-template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16, bool CAUSAL = false>
 cudaError_t launch_decode_t(const DecodeParams &dp, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                             size_t smem, cudaStream_t stream) {
-    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16>;
+    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel may begin its prologue while

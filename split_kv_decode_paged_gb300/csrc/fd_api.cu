@@ -84,6 +84,7 @@ using namespace fd;
 namespace {
 
 constexpr int kMaxStages = 8;
+constexpr int kMaxQLen = 64;  // query tokens per sequence (multi-token mode)
 constexpr int kMinStages = 2;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s limit on any device-side wait
 // Cost-model constants (in token-times of one CTA): fixed cost of one work
@@ -323,16 +324,21 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (!plan || !seq_lens_host) return FD_ERR_INVALID_ARG;
     fd_status st = validate_problem(problem);
     if (st != FD_OK) return st;
-    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0};
+    fd_plan_options opt = {0, 0, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0};
     if (options) opt = *options;
     if (opt.num_splits < 0 || opt.num_sms < 0 || opt.max_seq_len < 0 || opt.ctas_per_sm < 0 || opt.ctas_per_sm > 8 ||
         opt.split_margin_pct < 0 || opt.split_margin_pct > 100 ||
         (opt.tile_tokens != 0 && opt.tile_tokens != 64 && opt.tile_tokens != 128 && opt.tile_tokens != 256) ||
-        !hooks_valid(opt.timeout_us, opt.debug_stall_us, opt.debug_stall_role))
+        !hooks_valid(opt.timeout_us, opt.debug_stall_us, opt.debug_stall_role) || opt.q_len < 0 ||
+        opt.q_len > kMaxQLen)
         return FD_ERR_INVALID_ARG;
+    const int q_len = std::max(1, opt.q_len);
+    if (q_len > 1 && opt.shared_kv) return FD_ERR_UNSUPPORTED;
+    if ((long long)problem->B * q_len > kMaxBatch) return FD_ERR_UNSUPPORTED;
     // shared_kv: every q sequence attends KV row 0 (one block-table row, one
     // seq_lens entry): the B*G q rows of a KV head are sliced into items.
-    const int fold = opt.shared_kv ? problem->B : 1;
+    // q_len > 1: the q_len query tokens of a sequence fold onto its KV row.
+    const int fold = opt.shared_kv ? problem->B : q_len;
     const int kv_rows = opt.shared_kv ? 1 : problem->B;
     const double margin = (opt.split_margin_pct > 0 ? opt.split_margin_pct : kDefaultSplitMarginPct) / 100.0;
     const fd_problem &p = *problem;
@@ -344,6 +350,9 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         maxL = std::max<long long>(maxL, lens[b]);
     }
     const long long capL = std::max<long long>(maxL, opt.max_seq_len);
+    // shared memory of the dispatch tables follows the KV rows
+    fd_problem pm = p;
+    pm.B = kv_rows;
     if (capL > (long long)p.page_size * p.max_blocks_per_seq) return FD_ERR_INVALID_ARG;
 
     // The device is queried when present; planning for an explicit SM count
@@ -404,7 +413,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         for (int L : lens) sh.items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv * sh.nhg;
         sh.stages = 0;
         for (int s = kMaxStages; s >= kMinStages; --s) {
-            const size_t need = decode_smem_bytes(p, sh.ks, s);
+            const size_t need = decode_smem_bytes(pm, sh.ks, s);
             if ((long long)need <= smem_limit(cps)) {
                 sh.stages = s;
                 sh.smem = need;
@@ -419,9 +428,15 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     // 128 (16-bit K/V: always 128).
     const int cps_opt = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
     int tile_opt = opt.tile_tokens;
+    if (q_len > 1) {
+        // several causal query tokens per sequence: one CTA per SM, 128-token
+        // stages of 8 consumer warps (the shape built with the causal limits)
+        if ((opt.tile_tokens != 0 && opt.tile_tokens != 128) || cps_opt != 1) return FD_ERR_UNSUPPORTED;
+        tile_opt = 128;
+    }
     if (tile_opt == 0 && p.kv_dtype == FD_E4M3) {
         const KernelShape k256 = kernel_shape(p, 256, fold, cps_opt);
-        if (k256.tile == 256 && (long long)decode_smem_bytes(p, k256, 3) <= smem_limit(cps_opt)) tile_opt = 256;
+        if (k256.tile == 256 && (long long)decode_smem_bytes(pm, k256, 3) <= smem_limit(cps_opt)) tile_opt = 256;
     }
     Shape sh;
     if (!make_shape(tile_opt, cps_opt, sh)) return FD_ERR_UNSUPPORTED;
@@ -430,7 +445,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     // page ids).  Taken when the shape is left to the planner, the average
     // item attends fewer tokens than the threshold, there are enough items
     // for both CTAs of every SM, and two CTAs of that shape fit on an SM.
-    if (opt.tile_tokens == 0 && opt.ctas_per_sm == 0 && sh.items >= 4LL * sms) {
+    if (q_len == 1 && opt.tile_tokens == 0 && opt.ctas_per_sm == 0 && sh.items >= 4LL * sms) {
         long long tok = 0;
         for (int L : lens) tok += L;
         const double mean_item = (double)tok * p.Hkv * sh.nhg / (double)sh.items;
@@ -443,7 +458,11 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         const int tile2 = p.kv_dtype == FD_E4M3 ? 128 : 64;
         Shape s2;
         if (mean_item < limit && make_shape(tile2, 2, s2)) {
-            bool fits = s2.ks.nt == 1 || p.D == 64;  // register budget of two 5-warp CTAs
+            // Register budget of two 5-warp CTAs: three warps share one SM
+            // sub-partition's 16K registers, so at most 168 per thread.  Without
+            // a device, the shapes measured within it: one 8-head tile, or two
+            // at D = 64 for 16-bit K/V.
+            bool fits = s2.ks.nt == 1 || (p.D == 64 && p.kv_dtype != FD_E4M3);
             if (have_dev) {
                 int blocks = 0;
                 fits = decode_occupancy(p, s2.ks, s2.smem, &blocks) == cudaSuccess && blocks >= 2;
@@ -464,6 +483,8 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
 
     std::memset(plan, 0, sizeof(*plan));
     plan->problem = p;
+    plan->problem.B = kv_rows * fold;  // query rows
+    plan->q_len = q_len;
     plan->num_splits = slots;
     plan->chunk_tokens = C;
     plan->tile_tokens = tile;
@@ -481,7 +502,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     plan->timeout_us = opt.timeout_us;
     plan->debug_stall_us = opt.debug_stall_us;
     plan->debug_stall_role = opt.debug_stall_role;
-    const size_t rows = (size_t)p.B * p.Hq;
+    const size_t rows = (size_t)plan->problem.B * p.Hq;
     size_t off = 0;
     plan->ws_partial_o = off;
     off += align256(slots > 1 ? rows * slots * p.D * sizeof(float) : 0);
@@ -515,9 +536,12 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     if (workspace_bytes < plan->workspace_bytes) return FD_ERR_WORKSPACE_TOO_SMALL;
     const int fold = plan->row_fold;
     if (fold < 1 || plan->kv_rows < 1 || plan->kv_rows * fold != p.B || plan->head_subgroups < 1) return FD_ERR_INVALID_ARG;
+    const int q_len = std::max(1, plan->q_len);
+    if (q_len > kMaxQLen || (q_len > 1 && fold != q_len)) return FD_ERR_INVALID_ARG;
     if (fold > 1 && ex && (ex->cache_batch_idx || ex->cache_leftpad)) return FD_ERR_UNSUPPORTED;
     if (plan->ctas_per_sm < 0 || plan->ctas_per_sm > 8) return FD_ERR_INVALID_ARG;
     const KernelShape ks = kernel_shape(p, plan->tile_tokens, fold, std::max(1, plan->ctas_per_sm));
+    if (q_len > 1 && !(ks.consumer_warps == 8 && ks.subtiles == 1)) return FD_ERR_UNSUPPORTED;
     if (plan->head_subgroups != ((p.Hq / p.Hkv) * fold + 8 * ks.nt - 1) / (8 * ks.nt)) return FD_ERR_INVALID_ARG;
     if (plan->tile_tokens != ks.tile || plan->chunk_tokens < ks.tile || plan->chunk_tokens % ks.tile != 0 ||
         plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->stages < kMinStages ||
@@ -572,6 +596,7 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     dp.timeout_ns = plan->timeout_us > 0 ? (uint64_t)plan->timeout_us * 1000ull : kTimeoutNs;
     dp.stall_ns = (uint64_t)plan->debug_stall_us * 1000ull;
     dp.stall_role = plan->debug_stall_role;
+    dp.qn = q_len;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_decode(p, ks, dp, tmk, tmv, plan->grid_ctas, (size_t)plan->smem_bytes, s);

@@ -57,6 +57,7 @@ struct DecodeParams {
     uint64_t timeout_ns;       // limit of every device-side wait
     uint64_t stall_ns;         // test hook (0 = off): idle time of stall_role
     int stall_role;            // 1: producer before its first load; 2: consumers before the first release
+    int qn;                    // query tokens per KV row, causal among them (1: one-token decode)
 };
 
 struct MergeParams {
