@@ -694,8 +694,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         long long n_issued = 0;
         // One item of lookahead: the next item is claimed, and its first two
         // batches of page ids requested, while the current one streams.  The
-        // claim's atomic is issued as an item starts and its result read once
-        // the item's first tile is on its way.
+        // claim is made late, in the item's last tiles, so that an item is
+        // bound to the CTA that will be free first (a claim made as a long
+        // item starts would hold the next item back for that item's whole
+        // duration), while the stages still in flight cover the claim's
+        // round trip and the page-id requests.
         int next_item = (int)blockIdx.x;
         Item nx{};
         int npg0 = -1, npg1 = -1;
@@ -709,12 +712,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             const Item cur = nx;
             int pg_cur = npg0, pg_nxt = npg1;
             int claim_raw = 0;
-            if (lane == 0) claim_raw = atomicAdd(p.work_ctr, 1);
             const int b = cur.b, s = cur.s, kvh = cur.kvh, nsplit = cur.nsplit;
             const int t_begin = cur.t_begin, t_end = cur.t_end, ntok = cur.ntok, ntiles = cur.ntiles;
+            // Claim with the second-to-last tile and read it after the last
+            // one; with only two stages, one tile earlier each (the claim's
+            // round trip and the next item's page ids then have a tile's
+            // time more to arrive).
+            const int j_claim = NST >= 3 ? max(0, ntiles - 2) : max(0, ntiles - 3);
+            const int j_read = NST >= 3 ? ntiles - 1 : (ntiles >= 3 ? ntiles - 2 : 0);
             const int nbox = cur.nbox, box0 = cur.box0;
             int batch = 0;
             for (int j = 0; j < ntiles; ++j) {
+                if (j == j_claim && lane == 0) claim_raw = atomicAdd(p.work_ctr, 1);
                 const int kb = j * BPT;
                 if (kb >= (batch + 1) * 32) {
                     ++batch;
@@ -790,7 +799,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 }
                 ++n_issued;
                 if (++st == NST) { st = 0; ph ^= 1u; }
-                if (j == 0) {
+                if (j == j_read) {
                     next_item = (int)gridDim.x + __shfl_sync(0xffffffffu, claim_raw, 0);
                     if (next_item < total) {
                         nx = decode_item(next_item);
