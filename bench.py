@@ -6,8 +6,10 @@ One step = one fd_decode_paged call (split + merge) over one batch of the
 synthetic workload, inputs resident in HBM.  Workloads larger than 2x L2 are
 timed back to back between one CUDA-event pair on the launching stream; for
 smaller ones every timed step is preceded by an L2 flush (a write, then read,
-of 2x the L2 size) outside that step's event pair.  Prints ONE JSON line
-(rank 0).
+of 2x the L2 size) outside that step's event pair; in `per_config` their
+us per call is the marginal time of a call in a stream of (flush, call) pairs
+(an event pair around many pairs minus one around as many flushes), with the
+per-call event-pair mean beside it.  Prints ONE JSON line (rank 0).
 
 metric: achieved HBM GB/s of the decode call = algorithmic bytes (K+V of the
 live tokens, q, out, lse, live block-table entries, seq_lens, FP8 scales) /
@@ -224,6 +226,35 @@ def time_decode(wl, steps, warmup, flush, stream=None, **plan_opts):
     dec.check()
     ms = [a.elapsed_time(b) for a, b in ev]
     return ms, dec
+
+
+def flushed_marginal_us(wl, dec, flush, pairs=50, reps=5):
+    """Marginal time of one call in a stream of (L2 flush, call) pairs: one
+    event pair around `pairs` (flush, call) pairs minus one around `pairs`
+    flushes alone, divided by `pairs`; the median over `reps`.  Like the
+    back-to-back timing of the large workloads it leaves out the launch
+    latency that queued work hides, while every call still starts with a
+    cold L2 (an event pair around each call measures that latency too)."""
+    out = torch.empty_like(wl.q)
+    lse = torch.empty(wl.q.shape[:2], dtype=torch.float32, device=wl.q.device)
+    args = (wl.q, wl.k_pages, wl.v_pages, wl.block_table, wl.seq_lens)
+    kw = dict(k_scale=wl.k_scale, v_scale=wl.v_scale, out=out, lse=lse)
+    st = torch.cuda.current_stream()
+    res = []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(st)
+        for _ in range(pairs):
+            l2_flush(flush)
+            dec(*args, **kw)
+        e[1].record(st)
+        for _ in range(pairs):
+            l2_flush(flush)
+        e[2].record(st)
+        torch.cuda.synchronize()
+        res.append((e[0].elapsed_time(e[1]) - e[1].elapsed_time(e[2])) * 1e3 / pairs)
+    dec.check()
+    return statistics.median(res)
 
 
 def time_warm_and_graph(wl, dec, iters=50):
@@ -712,17 +743,20 @@ def per_call_spread(wl, dec, calls=50):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def config_entry(cfg, wl, ms, dec, peak, flushed, cpu=None, spread_ms=None):
+def config_entry(cfg, wl, ms, dec, peak, flushed, cpu=None, spread_ms=None, marginal_us=None):
     from split_kv_decode_paged_gb300 import workloads as W
     spec = W.CONFIGS[cfg]
     nbytes = W.algorithmic_bytes(spec, wl.seq_lens.cpu())
-    us = statistics.mean(ms) * 1e3
+    us = marginal_us if (flushed and marginal_us is not None) else statistics.mean(ms) * 1e3
     gbs = nbytes / us / 1e3
     plan = dec.plan
     e = {"workload": f"{spec.name}: B={spec.B}, Hq={spec.Hq}, Hkv={spec.Hkv}, D={spec.D}, {spec.kv} K/V, "
                      f"{spec.page_size}-token pages, lengths {tuple(spec.lens)} (seed {W.config_seed(cfg)})",
          "us_per_call": us, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak,
-         "timing": ("L2 flushed before every call, per-call event pairs (mean)" if flushed else
+         "timing": ("L2 flushed before every call; marginal time of a call in a stream of (flush, call) "
+                    "pairs: an event pair around 50 pairs minus one around 50 flushes (median of 5)"
+                    if flushed and marginal_us is not None else
+                    "L2 flushed before every call, per-call event pairs (mean)" if flushed else
                     "back to back, one event pair (mean)"),
          "traffic": profiled_traffic(CONFIG_TAGS[cfg]),
          "plan": {"num_splits": plan.num_splits, "chunk_tokens": plan.chunk_tokens, "tile_tokens": plan.tile_tokens,
@@ -731,6 +765,10 @@ def config_entry(cfg, wl, ms, dec, peak, flushed, cpu=None, spread_ms=None):
     e["us_median"], e["us_p10"], e["us_p90"] = sp
     if not flushed:
         e["spread_timing"] = "per-call event pairs, no flush (inputs > 2x L2)"
+    elif marginal_us is not None:
+        e["us_per_call_event_pair"] = statistics.mean(ms) * 1e3
+        e["spread_timing"] = ("per-call event pairs around each flushed call (they add the launch latency "
+                              "that the marginal time leaves out)")
     if cpu is not None:
         e["oracle"] = {"us_per_call": cpu["us_per_call"], "gbs": cpu["value"], "cores": cpu["cores"],
                        "sample": cpu["sample"]}
@@ -751,8 +789,9 @@ def per_config_block(args, dev, peak, flush_buf, flush_bytes, headline):
             ms, dec = time_decode(wl, 100 if big else 200, args.warmup, None if big else flush_buf)
             sp = per_call_spread(wl, dec) if big else None
         big = W.algorithmic_bytes(W.CONFIGS[c], wl.seq_lens.cpu()) > flush_bytes
+        marginal = None if big else flushed_marginal_us(wl, dec, flush_buf)
         cpu = None if args.no_cpu_baseline else cpu_baseline(wl.to("cpu"), target_s=args.per_config_cpu_seconds)
-        per[str(c)] = config_entry(c, wl, ms, dec, peak, not big, cpu, sp)
+        per[str(c)] = config_entry(c, wl, ms, dec, peak, not big, cpu, sp, marginal)
         if c != args.config:
             del wl, dec
             torch.cuda.empty_cache()
