@@ -158,7 +158,7 @@ __device__ __forceinline__ size_t q_row(const DecodeParams &p, int bkv, int kvh,
 // completed the last split: m_g = max m_i, w_i = exp(m_i - m_g),
 // O = sum w_i O_i / sum w_i d_i, lse = m_g + log(sum w_i d_i).
 // alpha: >= nrows*nsplit floats of shared memory.
-template <int NC>
+template <int NC, int kInFlight>
 __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int nrows, int qrows, int nsplit,
                             float *alpha, int warp, int lane, int D) {
     const int S = p.S;
@@ -202,14 +202,18 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int n
         return;
     }
     // Many splits: a warp per q row finds the weights (m and d read in one
-    // round), then the outputs in float4 groups with 8 split loads in flight.
+    // round), then the outputs in float4 groups with kInFlight split loads
+    // in flight (16 where the caller's state is dead here, else 8: the
+    // registers of the two-CTA shapes).
     for (int h = warp; h < nrows; h += NC) {
         const size_t row = q_row(p, b, kvh, hg, h, qrows);
         const float *pm = p.part_m + row * S;
         const float *pd = p.part_d + row * S;
         float mx = -INFINITY;
+        float d_lane = 0.f;  // d of split `lane`, requested with its m
         for (int s = lane; s < nsplit; s += 32) {
             const float ms = ldcg(pm + s);
+            if (s < 32) d_lane = ldcg(pd + s);
             alpha[h * nsplit + s] = ms;
             mx = fmaxf(mx, ms);
         }
@@ -220,7 +224,7 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int n
             const float ms = alpha[h * nsplit + s];
             const float a = (ms == -INFINITY) ? 0.f : __expf(ms - mx);
             alpha[h * nsplit + s] = a;
-            sum += a * ldcg(pd + s);
+            sum += a * (s < 32 ? d_lane : ldcg(pd + s));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -236,14 +240,14 @@ __device__ void merge_group(const DecodeParams &p, int b, int kvh, int hg, int n
         const float *po = p.part_o + row * S * D + d;
         const float *al = alpha + h * nsplit;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < nsplit; s0 += 8) {
-            float4 v[8];
+        for (int s0 = 0; s0 < nsplit; s0 += kInFlight) {
+            float4 v[kInFlight];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < kInFlight; ++k)
                 v[k] = (s0 + k < nsplit) ? __ldcg(reinterpret_cast<const float4 *>(po + (size_t)(s0 + k) * D))
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < kInFlight; ++k) {
                 const float a = (s0 + k < nsplit) ? al[s0 + k] : 0.f;
                 acc.x = fmaf(a, v[k].x, acc.x);
                 acc.y = fmaf(a, v[k].y, acc.y);
@@ -621,7 +625,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         auto decode_item = [&](int item) -> Item {
             Item it;
             int r2;
-            if (item < totalA) {
+            if (B == 1) {
+                // One KV row: its full chunks, then its partial chunk, so
+                // the chunk of item i is i / HG either way.
+                it.b = 0;
+                it.s = item / HG;
+                r2 = item - it.s * HG;
+            } else if (item < totalA) {
                 // The 32-row block by binary search over the block prefix,
                 // then the row by a warp scan of the block's item counts.
                 int lo = 0, hi = ((B + 31) >> 5) - 1;
@@ -1403,9 +1413,26 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             }
             named_bar_sync(1, NC * 32);
             if (*scr_flag) {
-                merge_group<NC>(p, mb, m_kvh, m_hg, m_nrows, QROWS, m_nsplit, scratch, warp, lane, D);
+                merge_group<NC, FP8 ? 8 : 16>(p, mb, m_kvh, m_hg, m_nrows, QROWS, m_nsplit, scratch, warp, lane, D);
                 if (tid == 0) atomicExch(p.merge_ctr + ((size_t)mb * p.Hkv + m_kvh) * p.nhg + m_hg, 0);
             }
+        }
+        // 16-bit K/V: the item's state and q fragments are spent; set them
+        // here (the next item's first stage sets them again) so that they
+        // are not live across the epilogue and the merge (fewer registers;
+        // measured faster for 16-bit K/V, not for E4M3).
+        if constexpr (!FP8)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+            for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) o[mi][n][r] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) qf[kk][n][0] = qf[kk][n][1] = 0u;
+            mrow[n][0] = mrow[n][1] = -INFINITY;
+            lrow[n][0] = lrow[n][1] = 0.f;
+            qd[n][0] = qd[n][1] = 1.f;
         }
         named_bar_sync(1, NC * 32);
     }
