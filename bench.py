@@ -293,20 +293,23 @@ def time_warm_and_graph(wl, dec, iters=50):
 
 
 def time_e2e(wl, dec, steps):
-    """End to end through the C ABI with host buffers (fd_decode_paged_host):
-    every step copies the packed pinned host block holding q, the block table
-    and seq_lens to the device (one copy) and runs the decode, which stores out
-    + lse into the packed pinned host output block (mapped for the device), all
-    inside the timed region; the timer stops after a stream synchronise, with
-    the results in host memory.  The paged K/V cache is state that lives in
-    HBM across steps."""
-    io = dec.host_step()
-    io.q.copy_(wl.q.cpu())
-    io.block_table.copy_(wl.block_table.cpu())
-    io.seq_lens.copy_(wl.seq_lens.cpu())
+    """End to end through the C ABI with host buffers: every step copies a
+    packed pinned host block holding q, the block table and seq_lens to the
+    device (one copy, fd_host_copy_in, on a copy stream where it overlaps the
+    previous step's decode: two sets of blocks in turn, HostPipeline) and runs
+    the decode (fd_decode_paged_staged), which stores out + lse into the packed
+    pinned host output block (mapped for the device), all inside the timed
+    region; the timer stops after a synchronise, with every step's results in
+    host memory.  The paged K/V cache is state that lives in HBM across
+    steps."""
+    pipe = dec.host_pipeline(2)
+    for io in pipe.ios:
+        io.q.copy_(wl.q.cpu())
+        io.block_table.copy_(wl.block_table.cpu())
+        io.seq_lens.copy_(wl.seq_lens.cpu())
 
     def step():
-        dec.step_host(io, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale)
+        pipe.submit(wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale)
 
     for _ in range(3):
         step()
@@ -317,7 +320,7 @@ def time_e2e(wl, dec, steps):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     dec.check()
-    return dt, io.layout.in_bytes, io.layout.out_bytes
+    return dt, pipe.ios[0].layout.in_bytes, pipe.ios[0].layout.out_bytes
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -942,8 +945,10 @@ def main():
         "e2e": None if args.quick else {"value": bytes_call / e2e_s / 1e9, "unit": "GB/s",
                                         "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
                                         "d2h_bytes_per_step": d2h,
-                                        "path": "fd_decode_paged_host: one pinned H2D copy of q + block table + "
-                                                "seq_lens, then the decode, whose kernel stores out + lse straight "
+                                        "path": "HostPipeline: per step one pinned H2D copy of q + block table "
+                                                "+ seq_lens (fd_host_copy_in, on a copy stream, overlapping the "
+                                                "previous step's decode; two block sets in turn), then the decode "
+                                                "(fd_decode_paged_staged), whose kernel stores out + lse straight "
                                                 "into the mapped pinned host block (d2h bytes cross during the "
                                                 "kernel, no separate copy)"},
         "gpu_launches": args.steps * (1 if plan.fuse_merge or plan.num_splits == 1 else 2),

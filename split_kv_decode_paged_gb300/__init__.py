@@ -15,7 +15,7 @@ from . import _lib
 from ._lib import (FD_BF16, FD_E4M3, FD_F16, FD_F32, FdError, fd_append_kv, fd_decode_paged, fd_merge_states,
                    fd_plan, fd_status_from_device, fd_status_string, make_problem)
 
-__all__ = ["PagedDecoder", "HostStep", "fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string",
+__all__ = ["PagedDecoder", "HostStep", "HostPipeline", "fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string",
            "fd_status_from_device", "make_problem", "FdError", "append_kv", "merge_states"]
 
 
@@ -66,6 +66,10 @@ class PagedDecoder:
         """Pinned host and device blocks for step_host (see HostStep)."""
         return HostStep(self)
 
+    def host_pipeline(self, depth=2):
+        """Host steps whose input copies overlap earlier decodes (see HostPipeline)."""
+        return HostPipeline(self, depth)
+
     def step_host(self, io, k_pages, v_pages, k_scale=None, v_scale=None, stream=None):
         """One decode step from host memory: io.q, io.block_table and
         io.seq_lens (pinned host views) are copied in with one copy, the
@@ -88,6 +92,48 @@ class PagedDecoder:
                 # before a call on any other stream can touch the workspace
                 torch.cuda.synchronize(self.device)
             raise FdError(fd_status_from_device(word), "device status")
+
+
+class HostPipeline:
+    """Decode steps from and to host memory with the input copy of each step
+    on a copy stream, where it overlaps the decode of the step before it:
+    `depth` sets of HostStep blocks used in turn (fd_host_copy_in on the copy
+    stream, fd_decode_paged_staged on the caller's stream, ordered by CUDA
+    events).  Fill io.q / io.block_table / io.seq_lens of `next_io()` before
+    `submit()`; read its io.out / io.lse once the stream has passed the step
+    (its event `done` has completed), and refill it no earlier than that."""
+
+    def __init__(self, dec: PagedDecoder, depth=2):
+        if depth < 1:
+            raise ValueError("depth must be at least 1")
+        self.dec = dec
+        self.ios = [HostStep(dec) for _ in range(depth)]
+        self.copy_stream = torch.cuda.Stream(device=dec.device)
+        self.copied = [torch.cuda.Event() for _ in range(depth)]
+        self.done = [None] * depth
+        self.k = 0
+
+    def next_io(self):
+        """The HostStep blocks the next submit() reads (its earlier step must be done)."""
+        return self.ios[self.k % len(self.ios)]
+
+    def submit(self, k_pages, v_pages, k_scale=None, v_scale=None, stream=None):
+        """Queue one step on the blocks of next_io(); returns them."""
+        i = self.k % len(self.ios)
+        io = self.ios[i]
+        main = stream if stream is not None else torch.cuda.current_stream(self.dec.device)
+        if self.done[i] is not None:
+            self.copy_stream.wait_event(self.done[i])  # the decode that last read dev_in
+        _lib.fd_host_copy_in(self.dec.plan, io.host_in, io.dev_in, self.copy_stream)
+        self.copied[i].record(self.copy_stream)
+        main.wait_event(self.copied[i])
+        _lib.fd_decode_paged_staged(self.dec.plan, io.dev_in, k_pages, v_pages, k_scale, v_scale, io.dev_out,
+                                    io.host_out, self.dec.workspace, self.dec.status, main)
+        ev = torch.cuda.Event()
+        ev.record(main)
+        self.done[i] = ev
+        self.k += 1
+        return io
 
 
 def append_kv(q_dtype, k_new, v_new, k_pages, v_pages, block_table, seq_lens, k_scale=None, v_scale=None,

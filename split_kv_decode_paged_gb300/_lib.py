@@ -1,7 +1,8 @@
 """ctypes binding of libfd.so (include/fd_api.h).  Argument marshalling only.
 
 Each function keeps the name of the C entry point it calls (fd_plan,
-fd_decode_paged, fd_decode_paged_ex, fd_decode_paged_host, fd_merge_states,
+fd_decode_paged, fd_decode_paged_ex, fd_decode_paged_host, fd_host_copy_in,
+fd_decode_paged_staged, fd_merge_states,
 fd_merge_two, fd_append_kv, fd_append_kv_rotary, ...).  Tensors are passed by
 data_ptr(); the stream is torch's current CUDA stream unless given.  No
 computation happens here and there is no fallback: if libfd.so is missing or
@@ -109,6 +110,10 @@ def load(path: str = LIB_PATH):
     L.fd_host_io_layout_for.argtypes = [ctypes.POINTER(FdPlan), ctypes.POINTER(FdHostIoLayout)]
     L.fd_decode_paged_host.restype = I
     L.fd_decode_paged_host.argtypes = [ctypes.POINTER(FdPlan), P, P, P, P, P, P, P, P, P, S, P, P]
+    L.fd_host_copy_in.restype = I
+    L.fd_host_copy_in.argtypes = [ctypes.POINTER(FdPlan), P, P, P]
+    L.fd_decode_paged_staged.restype = I
+    L.fd_decode_paged_staged.argtypes = [ctypes.POINTER(FdPlan), P, P, P, P, P, P, P, P, S, P, P]
     L.fd_status_string.restype = ctypes.c_char_p
     L.fd_status_string.argtypes = [I]
     L.fd_status_from_device.restype = I
@@ -408,3 +413,31 @@ def fd_decode_paged_host(plan: FdPlan, host_in, dev_in, k_pages, v_pages, k_scal
                                      _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged_host")
+
+
+def fd_host_copy_in(plan: FdPlan, host_in, dev_in, stream=None):
+    lay = fd_host_io_layout_for(plan)
+    a = _Args("fd_host_copy_in")
+    a.tensor("host_in", host_in, None, None, min_bytes=int(lay.in_bytes), host=True)
+    a.tensor("dev_in", dev_in, None, None, min_bytes=int(lay.in_bytes))
+    a.done()
+    rc = load().fd_host_copy_in(ctypes.byref(plan), _ptr(host_in), _ptr(dev_in), _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_host_copy_in")
+
+
+def fd_decode_paged_staged(plan: FdPlan, dev_in, k_pages, v_pages, k_scale, v_scale, dev_out, host_out, workspace,
+                           status=None, stream=None):
+    lay = fd_host_io_layout_for(plan)
+    a = _check_decode("fd_decode_paged_staged", plan, None, k_pages, v_pages, k_scale, v_scale, None, None, None,
+                      None, workspace, status, host_io=True)
+    a.tensor("dev_in", dev_in, None, None, min_bytes=int(lay.in_bytes))
+    a.tensor("host_out", host_out, None, None, min_bytes=int(lay.out_bytes), host=True)
+    a.tensor("dev_out", dev_out, None, None, min_bytes=int(lay.out_bytes))
+    a.done()
+    rc = load().fd_decode_paged_staged(ctypes.byref(plan), _ptr(dev_in), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
+                                       _ptr(v_scale), _ptr(dev_out), _ptr(host_out), _ptr(workspace),
+                                       int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                       _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_decode_paged_staged")

@@ -668,18 +668,26 @@ fd_status fd_host_io_layout_for(const fd_plan_t *plan, fd_host_io_layout *layout
     return FD_OK;
 }
 
-fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void *dev_in, const void *k_pages,
-                               const void *v_pages, const float *k_scale, const float *v_scale, void *dev_out,
-                               void *host_out, void *workspace, size_t workspace_bytes, int32_t *status_dev,
-                               void *stream) {
-    if (!plan || !host_in || !dev_in || !dev_out || !host_out) return FD_ERR_INVALID_ARG;
+fd_status fd_host_copy_in(const fd_plan_t *plan, const void *host_in, void *dev_in, void *stream) {
+    if (!plan || !host_in || !dev_in) return FD_ERR_INVALID_ARG;
+    if (!aligned(dev_in, 256)) return FD_ERR_INVALID_ARG;
+    fd_host_io_layout io;
+    fd_host_io_layout_for(plan, &io);
+    if (cudaMemcpyAsync(dev_in, host_in, io.in_bytes, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return FD_ERR_CUDA;
+    return FD_OK;
+}
+
+fd_status fd_decode_paged_staged(const fd_plan_t *plan, const void *dev_in, const void *k_pages, const void *v_pages,
+                                 const float *k_scale, const float *v_scale, void *dev_out, void *host_out,
+                                 void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream) {
+    if (!plan || !dev_in || !dev_out || !host_out) return FD_ERR_INVALID_ARG;
     if (!aligned(dev_in, 256) || !aligned(dev_out, 256)) return FD_ERR_INVALID_ARG;
     fd_host_io_layout io;
     fd_host_io_layout_for(plan, &io);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(dev_in, host_in, io.in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return FD_ERR_CUDA;
-    uint8_t *in = static_cast<uint8_t *>(dev_in);
+    const uint8_t *in = static_cast<const uint8_t *>(dev_in);
     // When the host output block is page-locked memory mapped for the device
     // (unified addressing), the kernel stores out and lse straight into it:
     // no device-to-host copy follows the decode.
@@ -702,6 +710,18 @@ fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void 
     if (!direct && cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return FD_ERR_CUDA;
     return FD_OK;
+}
+
+fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void *dev_in, const void *k_pages,
+                               const void *v_pages, const float *k_scale, const float *v_scale, void *dev_out,
+                               void *host_out, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                               void *stream) {
+    if (!plan || !host_in || !dev_in || !dev_out || !host_out) return FD_ERR_INVALID_ARG;
+    if (!aligned(dev_in, 256) || !aligned(dev_out, 256)) return FD_ERR_INVALID_ARG;
+    const fd_status r = fd_host_copy_in(plan, host_in, dev_in, stream);
+    if (r != FD_OK) return r;
+    return fd_decode_paged_staged(plan, dev_in, k_pages, v_pages, k_scale, v_scale, dev_out, host_out, workspace,
+                                  workspace_bytes, status_dev, stream);
 }
 
 fd_status fd_merge_states(const float *o_part, const float *m, const float *d, int B, int Hq, int S, int D,

@@ -28,7 +28,35 @@ def test_library_exports_every_declared_symbol(fdlib):
     assert {"fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string"} <= declared
     for name in declared:
         assert hasattr(fdlib, name), name
-    assert _lib.fd_api_version() == 3
+    assert _lib.fd_api_version() == 4
+
+
+def _declared_arg_counts():
+    counts = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            for name, args in re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fd_\w+)\s*\(([^)]*)\)\s*;", src, flags=re.M | re.S):
+                args = args.strip()
+                counts[name] = 0 if args in ("", "void") else args.count(",") + 1
+    return counts
+
+
+def test_binding_argument_counts_match_the_header(fdlib):
+    """Every entry point the binding declares argtypes for takes as many
+    arguments as its declaration in include/fd_api.h (a missing or extra
+    argument would shift every pointer after it)."""
+    counts = _declared_arg_counts()
+    lib = _lib.load()
+    checked = 0
+    for name, n in counts.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        checked += 1
+    assert checked >= 12
 
 
 def test_status_strings(fdlib):

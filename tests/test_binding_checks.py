@@ -143,6 +143,18 @@ def test_append_shapes(fdlib):
                                  torch.zeros((10, 16)))
 
 
+def test_staged_host_step_blocks(fdlib):
+    plan = _plan()
+    a = _args(plan)
+    lay = _lib.fd_host_io_layout_for(plan)
+    with pytest.raises(ValueError, match="host_in must hold at least"):
+        _lib.fd_host_copy_in(plan, torch.zeros(8, dtype=torch.uint8), torch.zeros(lay.in_bytes, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="dev_in must hold at least"):
+        _lib.fd_decode_paged_staged(plan, torch.zeros(8, dtype=torch.uint8), a["k_pages"], a["v_pages"], None, None,
+                                    torch.zeros(lay.out_bytes, dtype=torch.uint8),
+                                    torch.zeros(lay.out_bytes, dtype=torch.uint8), a["workspace"])
+
+
 def test_host_step_blocks(fdlib):
     plan = _plan()
     a = _args(plan)

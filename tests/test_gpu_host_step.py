@@ -76,3 +76,45 @@ def test_host_step_pageable_output_block_is_copied(fdlib):
     assert torch.equal(pageable[lay.out_offset:lay.out_offset + n_out], ref_out.cpu().view(torch.uint8).flatten())
     n_lse = ref_lse.numel() * 4
     assert torch.equal(pageable[lay.lse_offset:lay.lse_offset + n_lse], ref_lse.cpu().view(torch.uint8).flatten())
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3])
+def test_host_pipeline_steps_match_device_calls(fdlib, depth):
+    """HostPipeline (fd_host_copy_in on a copy stream, fd_decode_paged_staged
+    on the caller's stream, blocks used in turn): six steps with different
+    q rows each give exactly the results of fd_decode_paged on those rows."""
+    spec = CASES[0]
+    wl = W.make(spec, 33, "cpu")
+    g = wl.to("cuda")
+    dec = fd.PagedDecoder.for_pools(g.q, g.k_pages, g.v_pages, g.block_table, wl.seq_lens)
+    gen = torch.Generator().manual_seed(7)
+    qs = [torch.randn(wl.q.shape, generator=gen).to(wl.q.dtype) for _ in range(6)]
+    refs = []
+    for q in qs:
+        o, l = dec(q.cuda(), g.k_pages, g.v_pages, g.block_table, g.seq_lens, g.k_scale, g.v_scale)
+        refs.append((o.cpu(), l.cpu()))
+    torch.cuda.synchronize()
+    dec.check()
+    pipe = dec.host_pipeline(depth)
+    for io in pipe.ios:
+        io.block_table.copy_(wl.block_table)
+        io.seq_lens.copy_(wl.seq_lens)
+    pending = []
+    for k, q in enumerate(qs):
+        io = pipe.next_io()
+        slot = k % depth
+        if len(pending) == depth:  # the step that used these blocks: check it, then refill
+            kk, ev = pending.pop(0)
+            ev.synchronize()
+            assert torch.equal(io.out.view(torch.uint8), refs[kk][0].view(torch.uint8)), f"step {kk}"
+            assert torch.equal(io.lse.view(torch.int32), refs[kk][1].view(torch.int32)), f"step {kk}"
+        io.q.copy_(q)
+        io.out.fill_(float("nan"))
+        pipe.submit(g.k_pages, g.v_pages, g.k_scale, g.v_scale)
+        pending.append((k, pipe.done[slot]))
+    torch.cuda.synchronize()
+    dec.check()
+    for kk, _ in pending:
+        io = pipe.ios[kk % depth]
+        assert torch.equal(io.out.view(torch.uint8), refs[kk][0].view(torch.uint8)), f"step {kk}"
+        assert torch.equal(io.lse.view(torch.int32), refs[kk][1].view(torch.int32)), f"step {kk}"
