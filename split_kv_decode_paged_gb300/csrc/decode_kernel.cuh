@@ -992,7 +992,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
 
         // The warp's SUBT sub-tiles of 16 tokens (tile rows r0 .. r0+15 with
-        // r0 = (warp*SUBT + sub)*16, each inside box r0 / boxr) share one
+        // r0 = (sub*NC + warp)*16, each inside box r0 / boxr: sub-tiles are
+        // dealt to the warps in turn, so a ragged last tile leaves every warp
+        // about the same number of valid rows) share one
         // online-softmax step: scores of every sub-tile, one check of the
         // reference maxima (and, when needed, one reduction and O rescale),
         // then P.V of every sub-tile.  Valid rows of a sub-tile: [ll, nl).
@@ -1000,7 +1002,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         bool any_act = false;
 #pragma unroll
         for (int sub = 0; sub < SUBT; ++sub) {
-            const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+            const int r0 = (sub * NC + warp) * kTokensPerWarp;
             nl[sub] = max(0, min(kTokensPerWarp, nvalid - r0));
             ll[sub] = max(0, vlo - r0);
             any_act |= nl[sub] > ll[sub];
@@ -1013,7 +1015,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             float sv[SUBT][NT][4];
 #pragma unroll
             for (int sub = 0; sub < SUBT; ++sub) {
-                const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+                const int r0 = (sub * NC + warp) * kTokensPerWarp;
                 const uint32_t kbox = kbase + (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
                 const int row_a = r0 % p.boxr + (lane & 7) + ((lane >> 3) & 1) * 8;
                 float s2[NT][4];
@@ -1193,7 +1195,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 #pragma unroll
             for (int sub = 0; sub < SUBT; ++sub) {
                 if (!(nl[sub] > ll[sub])) continue;
-                const int r0 = (warp * SUBT + sub) * kTokensPerWarp;
+                const int r0 = (sub * NC + warp) * kTokensPerWarp;
                 const int rib = r0 % p.boxr;
                 const uint32_t vbox = vbase + (uint32_t)((r0 / p.boxr) * NHALF) * hstride;
                 // Rows outside [ll, nl) may hold any bits (stale or NaN):
