@@ -372,25 +372,32 @@ fd_status fd_decode_paged_host(const fd_plan_t *plan, const void *host_in, void 
                                void *workspace, size_t workspace_bytes, int32_t *status_dev,
                                void *stream);
 
-/* The two halves of fd_decode_paged_host, for callers that queue them on
+/* The parts of fd_decode_paged_host, for callers that queue them on
  * different streams: the input copy of one step on a copy stream while the
- * decode of the previous step runs (two input blocks in turn; the caller
- * orders each decode after its copy, and each copy into dev_in after the
- * decode that last read it, e.g. with CUDA events).
+ * decode of the previous step runs, and (optionally) the output copy of a
+ * step on a copy stream while the next one decodes (several block sets in
+ * turn; the caller orders each decode after its input copy, each input copy
+ * into dev_in after the decode that last read it, each output copy after its
+ * decode, and each decode into dev_out after the output copy that last read
+ * it, e.g. with CUDA events).
  *
  * fd_host_copy_in: queue the copy of host_in (in_bytes) to dev_in on
  *   `stream`.  Arguments as fd_decode_paged_host.  FD_ERR_INVALID_ARG on NULL
  *   blocks or an unaligned dev_in; FD_ERR_CUDA when the copy cannot be queued.
  * fd_decode_paged_staged: the decode of fd_decode_paged_host from an input
  *   block already in dev_in (its copy queued before, in stream order or behind
- *   an event), with the same output handling (stores straight into a mapped
- *   host_out, else a copy from dev_out).  Arguments and errors as
- *   fd_decode_paged_host. */
+ *   an event).  host_out as fd_decode_paged_host (stores straight into a
+ *   mapped block, else a copy from dev_out), or NULL: the results stay in
+ *   dev_out.  Other arguments and errors as fd_decode_paged_host.
+ * fd_host_copy_out: queue the copy of dev_out (out_bytes) to host_out on
+ *   `stream`.  FD_ERR_INVALID_ARG on NULL blocks or an unaligned dev_out;
+ *   FD_ERR_CUDA when the copy cannot be queued. */
 fd_status fd_host_copy_in(const fd_plan_t *plan, const void *host_in, void *dev_in, void *stream);
 fd_status fd_decode_paged_staged(const fd_plan_t *plan, const void *dev_in, const void *k_pages,
                                  const void *v_pages, const float *k_scale, const float *v_scale,
                                  void *dev_out, void *host_out, void *workspace, size_t workspace_bytes,
                                  int32_t *status_dev, void *stream);
+fd_status fd_host_copy_out(const fd_plan_t *plan, const void *dev_out, void *host_out, void *stream);
 
 /* Map a device status word to a status code (FD_OK when zero). */
 fd_status fd_status_from_device(int32_t status_word);

@@ -66,9 +66,9 @@ class PagedDecoder:
         """Pinned host and device blocks for step_host (see HostStep)."""
         return HostStep(self)
 
-    def host_pipeline(self, depth=2):
-        """Host steps whose input copies overlap earlier decodes (see HostPipeline)."""
-        return HostPipeline(self, depth)
+    def host_pipeline(self, depth=2, direct_out=True):
+        """Host steps whose copies overlap other steps' decodes (see HostPipeline)."""
+        return HostPipeline(self, depth, direct_out)
 
     def step_host(self, io, k_pages, v_pages, k_scale=None, v_scale=None, stream=None):
         """One decode step from host memory: io.q, io.block_table and
@@ -97,20 +97,26 @@ class PagedDecoder:
 class HostPipeline:
     """Decode steps from and to host memory with the input copy of each step
     on a copy stream, where it overlaps the decode of the step before it:
-    `depth` sets of HostStep blocks used in turn (fd_host_copy_in on the copy
-    stream, fd_decode_paged_staged on the caller's stream, ordered by CUDA
-    events).  Fill io.q / io.block_table / io.seq_lens of `next_io()` before
-    `submit()`; read its io.out / io.lse once the stream has passed the step
-    (its event `done` has completed), and refill it no earlier than that."""
+    `depth` sets of HostStep blocks used in turn (fd_host_copy_in on the input
+    copy stream, fd_decode_paged_staged on the caller's stream, ordered by
+    CUDA events).  direct_out=True: the kernel stores out and lse straight
+    into the mapped pinned output block; False: into the device block, and
+    fd_host_copy_out on an output copy stream moves them while the next step
+    decodes.  Fill io.q / io.block_table / io.seq_lens of `next_io()` before
+    `submit()`; read its io.out / io.lse once the step's event `done[i]` has
+    completed, and refill it no earlier than that."""
 
-    def __init__(self, dec: PagedDecoder, depth=2):
+    def __init__(self, dec: PagedDecoder, depth=2, direct_out=True):
         if depth < 1:
             raise ValueError("depth must be at least 1")
         self.dec = dec
+        self.direct_out = direct_out
         self.ios = [HostStep(dec) for _ in range(depth)]
-        self.copy_stream = torch.cuda.Stream(device=dec.device)
+        self.in_stream = torch.cuda.Stream(device=dec.device)
+        self.out_stream = torch.cuda.Stream(device=dec.device)
         self.copied = [torch.cuda.Event() for _ in range(depth)]
-        self.done = [None] * depth
+        self.decoded = [None] * depth  # the decode that last read dev_in / wrote dev_out of set i
+        self.done = [None] * depth     # set i's last step complete (results in host memory)
         self.k = 0
 
     def next_io(self):
@@ -121,17 +127,29 @@ class HostPipeline:
         """Queue one step on the blocks of next_io(); returns them."""
         i = self.k % len(self.ios)
         io = self.ios[i]
+        plan = self.dec.plan
         main = stream if stream is not None else torch.cuda.current_stream(self.dec.device)
-        if self.done[i] is not None:
-            self.copy_stream.wait_event(self.done[i])  # the decode that last read dev_in
-        _lib.fd_host_copy_in(self.dec.plan, io.host_in, io.dev_in, self.copy_stream)
-        self.copied[i].record(self.copy_stream)
+        if self.decoded[i] is not None:
+            self.in_stream.wait_event(self.decoded[i])  # the decode that last read dev_in
+        _lib.fd_host_copy_in(plan, io.host_in, io.dev_in, self.in_stream)
+        self.copied[i].record(self.in_stream)
         main.wait_event(self.copied[i])
-        _lib.fd_decode_paged_staged(self.dec.plan, io.dev_in, k_pages, v_pages, k_scale, v_scale, io.dev_out,
-                                    io.host_out, self.dec.workspace, self.dec.status, main)
-        ev = torch.cuda.Event()
-        ev.record(main)
-        self.done[i] = ev
+        if not self.direct_out and self.done[i] is not None:
+            main.wait_event(self.done[i])  # the output copy that last read dev_out
+        _lib.fd_decode_paged_staged(plan, io.dev_in, k_pages, v_pages, k_scale, v_scale, io.dev_out,
+                                    io.host_out if self.direct_out else None, self.dec.workspace,
+                                    self.dec.status, main)
+        dec_ev = torch.cuda.Event()
+        dec_ev.record(main)
+        self.decoded[i] = dec_ev
+        if self.direct_out:
+            self.done[i] = dec_ev
+        else:
+            self.out_stream.wait_event(dec_ev)
+            _lib.fd_host_copy_out(plan, io.dev_out, io.host_out, self.out_stream)
+            ev = torch.cuda.Event()
+            ev.record(self.out_stream)
+            self.done[i] = ev
         self.k += 1
         return io
 

@@ -2,7 +2,7 @@
 
 Each function keeps the name of the C entry point it calls (fd_plan,
 fd_decode_paged, fd_decode_paged_ex, fd_decode_paged_host, fd_host_copy_in,
-fd_decode_paged_staged, fd_merge_states,
+fd_decode_paged_staged, fd_host_copy_out, fd_merge_states,
 fd_merge_two, fd_append_kv, fd_append_kv_rotary, ...).  Tensors are passed by
 data_ptr(); the stream is torch's current CUDA stream unless given.  No
 computation happens here and there is no fallback: if libfd.so is missing or
@@ -114,6 +114,8 @@ def load(path: str = LIB_PATH):
     L.fd_host_copy_in.argtypes = [ctypes.POINTER(FdPlan), P, P, P]
     L.fd_decode_paged_staged.restype = I
     L.fd_decode_paged_staged.argtypes = [ctypes.POINTER(FdPlan), P, P, P, P, P, P, P, P, S, P, P]
+    L.fd_host_copy_out.restype = I
+    L.fd_host_copy_out.argtypes = [ctypes.POINTER(FdPlan), P, P, P]
     L.fd_status_string.restype = ctypes.c_char_p
     L.fd_status_string.argtypes = [I]
     L.fd_status_from_device.restype = I
@@ -432,7 +434,7 @@ def fd_decode_paged_staged(plan: FdPlan, dev_in, k_pages, v_pages, k_scale, v_sc
     a = _check_decode("fd_decode_paged_staged", plan, None, k_pages, v_pages, k_scale, v_scale, None, None, None,
                       None, workspace, status, host_io=True)
     a.tensor("dev_in", dev_in, None, None, min_bytes=int(lay.in_bytes))
-    a.tensor("host_out", host_out, None, None, min_bytes=int(lay.out_bytes), host=True)
+    a.tensor("host_out", host_out, None, None, min_bytes=int(lay.out_bytes), host=True, optional=True)
     a.tensor("dev_out", dev_out, None, None, min_bytes=int(lay.out_bytes))
     a.done()
     rc = load().fd_decode_paged_staged(ctypes.byref(plan), _ptr(dev_in), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
@@ -441,3 +443,14 @@ def fd_decode_paged_staged(plan: FdPlan, dev_in, k_pages, v_pages, k_scale, v_sc
                                        _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged_staged")
+
+
+def fd_host_copy_out(plan: FdPlan, dev_out, host_out, stream=None):
+    lay = fd_host_io_layout_for(plan)
+    a = _Args("fd_host_copy_out")
+    a.tensor("dev_out", dev_out, None, None, min_bytes=int(lay.out_bytes))
+    a.tensor("host_out", host_out, None, None, min_bytes=int(lay.out_bytes), host=True)
+    a.done()
+    rc = load().fd_host_copy_out(ctypes.byref(plan), _ptr(dev_out), _ptr(host_out), _stream(stream))
+    if rc != FD_OK:
+        raise FdError(rc, "fd_host_copy_out")

@@ -682,7 +682,7 @@ fd_status fd_host_copy_in(const fd_plan_t *plan, const void *host_in, void *dev_
 fd_status fd_decode_paged_staged(const fd_plan_t *plan, const void *dev_in, const void *k_pages, const void *v_pages,
                                  const float *k_scale, const float *v_scale, void *dev_out, void *host_out,
                                  void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream) {
-    if (!plan || !dev_in || !dev_out || !host_out) return FD_ERR_INVALID_ARG;
+    if (!plan || !dev_in || !dev_out) return FD_ERR_INVALID_ARG;
     if (!aligned(dev_in, 256) || !aligned(dev_out, 256)) return FD_ERR_INVALID_ARG;
     fd_host_io_layout io;
     fd_host_io_layout_for(plan, &io);
@@ -694,11 +694,11 @@ fd_status fd_decode_paged_staged(const fd_plan_t *plan, const void *dev_in, cons
     uint8_t *out = static_cast<uint8_t *>(dev_out);
     bool direct = false;
     cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, host_out) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+    if (host_out && cudaPointerGetAttributes(&attr, host_out) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
         attr.devicePointer != nullptr && aligned(attr.devicePointer, 256)) {
         out = static_cast<uint8_t *>(attr.devicePointer);
         direct = true;
-    } else {
+    } else if (host_out) {
         cudaGetLastError();  // a pageable pointer is not an error here
     }
     const fd_status r = fd_decode_paged(plan, in + io.q_offset, k_pages, v_pages, k_scale, v_scale,
@@ -707,7 +707,19 @@ fd_status fd_decode_paged_staged(const fd_plan_t *plan, const void *dev_in, cons
                                         out + io.out_offset, reinterpret_cast<float *>(out + io.lse_offset),
                                         workspace, workspace_bytes, status_dev, stream);
     if (r != FD_OK) return r;
-    if (!direct && cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (host_out && !direct &&
+        cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return FD_OK;
+}
+
+fd_status fd_host_copy_out(const fd_plan_t *plan, const void *dev_out, void *host_out, void *stream) {
+    if (!plan || !dev_out || !host_out) return FD_ERR_INVALID_ARG;
+    if (!aligned(dev_out, 256)) return FD_ERR_INVALID_ARG;
+    fd_host_io_layout io;
+    fd_host_io_layout_for(plan, &io);
+    if (cudaMemcpyAsync(host_out, dev_out, io.out_bytes, cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return FD_ERR_CUDA;
     return FD_OK;
 }

@@ -155,6 +155,15 @@ def test_staged_host_step_blocks(fdlib):
                                     torch.zeros(lay.out_bytes, dtype=torch.uint8), a["workspace"])
 
 
+def test_host_copy_out_blocks(fdlib):
+    plan = _plan()
+    lay = _lib.fd_host_io_layout_for(plan)
+    with pytest.raises(ValueError, match="dev_out must hold at least"):
+        _lib.fd_host_copy_out(plan, torch.zeros(8, dtype=torch.uint8), torch.zeros(lay.out_bytes, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="host_out must hold at least"):
+        _lib.fd_host_copy_out(plan, torch.zeros(lay.out_bytes, dtype=torch.uint8), torch.zeros(8, dtype=torch.uint8))
+
+
 def test_host_step_blocks(fdlib):
     plan = _plan()
     a = _args(plan)

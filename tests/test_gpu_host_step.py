@@ -78,11 +78,14 @@ def test_host_step_pageable_output_block_is_copied(fdlib):
     assert torch.equal(pageable[lay.lse_offset:lay.lse_offset + n_lse], ref_lse.cpu().view(torch.uint8).flatten())
 
 
+@pytest.mark.parametrize("direct_out", [True, False], ids=["mapped-out", "copied-out"])
 @pytest.mark.parametrize("depth", [1, 2, 3])
-def test_host_pipeline_steps_match_device_calls(fdlib, depth):
+def test_host_pipeline_steps_match_device_calls(fdlib, depth, direct_out):
     """HostPipeline (fd_host_copy_in on a copy stream, fd_decode_paged_staged
-    on the caller's stream, blocks used in turn): six steps with different
-    q rows each give exactly the results of fd_decode_paged on those rows."""
+    on the caller's stream, fd_host_copy_out on another copy stream unless the
+    kernel stores into the mapped block, blocks used in turn): six steps with
+    different q rows each give exactly the results of fd_decode_paged on those
+    rows."""
     spec = CASES[0]
     wl = W.make(spec, 33, "cpu")
     g = wl.to("cuda")
@@ -95,7 +98,7 @@ def test_host_pipeline_steps_match_device_calls(fdlib, depth):
         refs.append((o.cpu(), l.cpu()))
     torch.cuda.synchronize()
     dec.check()
-    pipe = dec.host_pipeline(depth)
+    pipe = dec.host_pipeline(depth, direct_out)
     for io in pipe.ios:
         io.block_table.copy_(wl.block_table)
         io.seq_lens.copy_(wl.seq_lens)
