@@ -86,6 +86,7 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kMaxQLen = 64;  // query tokens per sequence (multi-token mode)
 constexpr int kMinStages = 2;
+constexpr int kSmallGridItemTokens = 1024;  // small grids: two CTAs per SM for items up to this long
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s limit on any device-side wait
 // Cost-model constants (in token-times of one CTA): fixed cost of one work
 // item (epilogue + pipeline hand-over) and the relative margin within which
@@ -385,7 +386,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         size_t smem = 0;
         long long items = 0;
     };
-    auto make_shape = [&](int tile_opt, int cps, Shape &sh) -> bool {
+    auto make_shape = [&](int tile_opt, int cps, Shape &sh, int force_splits = 0) -> bool {
         sh.ks = kernel_shape(p, tile_opt, fold, cps);
         sh.cps = cps;
         const int tile = sh.ks.tile;
@@ -396,8 +397,9 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         pk.Hkv = p.Hkv * sh.nhg;
         const int P = sms * cps;
         int C;
-        if (opt.num_splits > 0) {
-            const int S = std::min(opt.num_splits, kMaxSplits);
+        const int S_opt = force_splits > 0 ? force_splits : opt.num_splits;
+        if (S_opt > 0) {
+            const int S = std::min(S_opt, kMaxSplits);
             C = std::max(tile, round_up((std::max<long long>(maxL, 1) + S - 1) / S, tile));
         } else {
             C = choose_chunk(lens, pk, P, tile, margin);
@@ -469,6 +471,43 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
                 cudaGetLastError();
             }
             if (fits) sh = s2;
+        }
+    }
+    // Small grids: fewer work items than SMs leave SMs idle and each CTA's
+    // start-up, ramp and tail exposed.  Two CTAs per SM with the most splits
+    // whose items still fit the 2 x SMs slots halve the items and double the
+    // streams; taken when the items stay short (at most kSmallGridItemTokens)
+    // or the TMA boxes are small (at most 2 KB: one producer issues them too
+    // slowly to keep an SM busy).  Measured on GB300 (same GPU, marginal time
+    // per L2-flushed call): one sequence of 32 MHA heads, f16, 16-token pages,
+    // D = 128: 2048 tokens -9.2%, 4096 tokens -2.2%, 16384 tokens +7% when
+    // forced (so left alone by the item-length test); D = 64, 8192 tokens
+    // (2 KB boxes) -16.6%; two sequences of 16 heads, 4096 tokens -0.6%.
+    // Chunks keep the planner's floor (sequences of at most 2 x kMinChunkTokens
+    // are not split, nor cut below kMinChunkTokens).
+    if (q_len == 1 && opt.tile_tokens == 0 && opt.ctas_per_sm == 0 && opt.num_splits == 0 && sh.cps == 1 &&
+        sh.items < sms && maxL > 2 * kMinChunkTokens) {
+        const int tile2 = p.kv_dtype == FD_E4M3 ? 128 : 64;
+        int best_S = 0;
+        for (int S = std::min(kMaxSplits, 2 * sms); S >= 1 && best_S == 0; --S) {
+            Shape t;
+            if (make_shape(tile2, 2, t, S) && t.items <= 2LL * sms && (t.slots == 1 || t.C >= kMinChunkTokens))
+                best_S = S;
+        }
+        Shape s2;
+        if (best_S > 0 && make_shape(tile2, 2, s2, best_S) && s2.items > sh.items) {
+            long long tok = 0;
+            for (int L : lens) tok += L;
+            const double mean_item = (double)tok * p.Hkv * s2.nhg / (double)s2.items;
+            const int boxr2 = std::gcd(p.page_size, s2.ks.tile);
+            const long long box_bytes = (long long)boxr2 * p.D * (p.kv_dtype == FD_E4M3 ? 1 : 2);
+            bool fits = s2.ks.nt == 1 || (p.D == 64 && p.kv_dtype != FD_E4M3);
+            if (have_dev) {
+                int blocks = 0;
+                fits = decode_occupancy(p, s2.ks, s2.smem, &blocks) == cudaSuccess && blocks >= 2;
+                cudaGetLastError();
+            }
+            if (fits && (mean_item <= kSmallGridItemTokens || box_bytes <= 2048)) sh = s2;
         }
     }
     const KernelShape ks = sh.ks;
