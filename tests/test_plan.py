@@ -155,6 +155,27 @@ def test_short_items_take_two_ctas_per_sm(kv, ps, B, L, want_two):
         assert plan.ctas_per_sm == 1 and plan.grid_ctas <= 152 and plan.tile_tokens >= 128
 
 
+@pytest.mark.parametrize("B,H,D,L,kv,want_two,want_splits", [
+    (1, 32, 128, 4096, torch.float16, True, 8),      # single-sequence MHA: 8 splits of 512
+    (1, 32, 128, 2048, torch.float16, True, 8),      # 8 splits of 256
+    (1, 32, 64, 8192, torch.float16, True, 9),       # 2 KB boxes: 9 splits of 960
+    (1, 32, 128, 16384, torch.float16, False, 4),    # long items, 4 KB boxes: one CTA per SM
+    (1, 4, 64, 256, torch.float16, False, 1),        # short sequence: not split
+    (1, 32, 128, 1024, torch.float16, False, 4),     # at most 2 x 256 tokens would remain per item
+])
+def test_small_grids_take_two_ctas_per_sm(fdlib, B, H, D, L, kv, want_two, want_splits):
+    """Fewer work items than SMs: two CTAs per SM with the most splits whose
+    items fit the 2 x SM slots, when the items stay short or the boxes small."""
+    prob = _prob(B, H, H, L, D=D, dt=kv)
+    plan = _lib.fd_plan(prob, [L] * B, num_sms=152)
+    assert plan.num_splits == want_splits
+    if want_two:
+        assert plan.ctas_per_sm == 2 and plan.tile_tokens == 64
+        assert plan.work_items_hint <= 2 * 152 and plan.chunk_tokens >= 256
+    else:
+        assert plan.ctas_per_sm == 1
+
+
 def test_short_items_rule_respects_explicit_options_and_registers(fdlib):
     prob = _lib.make_problem(512, 32, 8, 128, 16, 64, 512 * 64, torch.bfloat16, torch.bfloat16)
     assert _lib.fd_plan(prob, [256] * 512, num_sms=152, tile_tokens=128).tile_tokens == 128
