@@ -485,10 +485,13 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     // (2 KB boxes) -16.6%; two sequences of 16 heads, 4096 tokens -0.6%.
     // Chunks keep the planner's floor (sequences of at most 2 x kMinChunkTokens
     // are not split, nor cut below kMinChunkTokens).
-    // 16-bit K/V only (measured there).
-    if (q_len == 1 && p.kv_dtype != FD_E4M3 && opt.tile_tokens == 0 && opt.ctas_per_sm == 0 &&
-        opt.num_splits == 0 && sh.cps == 1 && sh.items < sms && maxL > 2 * kMinChunkTokens) {
-        const int tile2 = 64;
+    // E4M3 K/V (128-token stages of 4 warps x 2 sub-tiles, same GPU): one
+    // sequence of 32 MHA heads, 16-token pages, 2048 / 4096 tokens -9.6% /
+    // -19%; 128-token pages, 4096 tokens -10%; two sequences of 16 heads,
+    // 64-token pages, 8192 tokens -3%.
+    if (q_len == 1 && opt.tile_tokens == 0 && opt.ctas_per_sm == 0 && opt.num_splits == 0 && sh.cps == 1 &&
+        sh.items < sms && maxL > 2 * kMinChunkTokens) {
+        const int tile2 = p.kv_dtype == FD_E4M3 ? 128 : 64;
         int best_S = 0;
         for (int S = std::min(kMaxSplits, 2 * sms); S >= 1 && best_S == 0; --S) {
             Shape t;
@@ -501,8 +504,8 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
             for (int L : lens) tok += L;
             const double mean_item = (double)tok * p.Hkv * s2.nhg / (double)s2.items;
             const int boxr2 = std::gcd(p.page_size, s2.ks.tile);
-            const long long box_bytes = (long long)boxr2 * p.D * 2;
-            bool fits = s2.ks.nt == 1 || p.D == 64;
+            const long long box_bytes = (long long)boxr2 * p.D * (p.kv_dtype == FD_E4M3 ? 1 : 2);
+            bool fits = s2.ks.nt == 1 || (p.D == 64 && p.kv_dtype != FD_E4M3);
             if (have_dev) {
                 int blocks = 0;
                 fits = decode_occupancy(p, s2.ks, s2.smem, &blocks) == cudaSuccess && blocks >= 2;

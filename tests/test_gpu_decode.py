@@ -273,7 +273,8 @@ def test_fp8_two_ctas_128_token_stages(fdlib, Hq, D, splits, fuse):
 @pytest.mark.parametrize("kv,q,D,H,L,B", [("f16", "f16", 64, 32, 8192, 1),
                                           ("f16", "f16", 128, 32, 2048, 1),
                                           ("bf16", "bf16", 128, 16, 4096, 2),
-                                          ("f16", "f16", 128, 32, 3000, 1)])
+                                          ("f16", "f16", 128, 32, 3000, 1),
+                                          ("e4m3", "bf16", 128, 32, 3000, 1)])
 def test_small_grids_two_ctas_per_sm(fdlib, kv, q, D, H, L, B):
     """Fewer items than SMs: the planner's small-grid shape (two CTAs per SM,
     64-token stages, more splits, fused merge) against the oracle on every
@@ -281,4 +282,5 @@ def test_small_grids_two_ctas_per_sm(fdlib, kv, q, D, H, L, B):
     ragged."""
     spec = _spec(f"small grid {kv} D={D} L={L}", B, H, H, D, 16, kv, q, [L] * B, pool=("factor", 2.0))
     err, dec = _run_and_check(spec, 61 + D + L)
-    assert dec.plan.ctas_per_sm == 2 and dec.plan.tile_tokens == 64 and dec.plan.num_splits > 4
+    assert dec.plan.ctas_per_sm == 2 and dec.plan.num_splits > 4
+    assert dec.plan.tile_tokens == (128 if kv == "e4m3" else 64)

@@ -162,15 +162,16 @@ def test_short_items_take_two_ctas_per_sm(kv, ps, B, L, want_two):
     (1, 32, 128, 16384, torch.float16, False, 4),    # long items, 4 KB boxes: one CTA per SM
     (1, 4, 64, 256, torch.float16, False, 1),        # short sequence: not split
     (1, 32, 128, 1024, torch.float16, False, 4),     # at most 2 x 256 tokens would remain per item
+    (1, 32, 128, 4096, torch.float8_e4m3fn, True, 8),  # E4M3: 128-token stages of 4 warps x 2
 ])
 def test_small_grids_take_two_ctas_per_sm(fdlib, B, H, D, L, kv, want_two, want_splits):
     """Fewer work items than SMs: two CTAs per SM with the most splits whose
     items fit the 2 x SM slots, when the items stay short or the boxes small."""
-    prob = _prob(B, H, H, L, D=D, dt=kv)
+    prob = _prob(B, H, H, L, D=D, dt=torch.bfloat16 if kv == torch.float8_e4m3fn else kv, kv=kv)
     plan = _lib.fd_plan(prob, [L] * B, num_sms=152)
     assert plan.num_splits == want_splits
     if want_two:
-        assert plan.ctas_per_sm == 2 and plan.tile_tokens == 64
+        assert plan.ctas_per_sm == 2 and plan.tile_tokens == (128 if kv == torch.float8_e4m3fn else 64)
         assert plan.work_items_hint <= 2 * 152 and plan.chunk_tokens >= 256
     else:
         assert plan.ctas_per_sm == 1
