@@ -104,7 +104,7 @@ constexpr int kDefaultSplitMarginPct = 2;
 // K/V switch below 2048 tokens per item when the default shape has 256-token
 // stages, and always otherwise (16-token pages or very large batches, where
 // one producer per SM issuing 2 KB boxes is the limit).
-constexpr double kShortItemTokens = 768.0;
+constexpr double kShortItemTokens = 1024.0;
 constexpr double kShortItemTokensShallow = 1280.0;
 constexpr double kShortItemTokensE4m3 = 2048.0;
 

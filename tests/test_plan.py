@@ -129,6 +129,7 @@ SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per 
 @pytest.mark.parametrize("kv,ps,B,L,want_two", [
     (torch.bfloat16, 16, 512, 256, True),      # short items: two CTAs per SM, 64-token stages
     (torch.bfloat16, 16, 512, 512, True),
+    (torch.bfloat16, 16, 512, 768, True),
     (torch.bfloat16, 16, 512, 1024, False),    # long enough for the default shape
     (torch.bfloat16, 16, 2048, 1024, True),    # ... unless the default lost a stage to its tables
     (torch.bfloat16, 16, 2048, 2048, False),
