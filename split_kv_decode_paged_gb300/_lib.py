@@ -127,17 +127,16 @@ def load(path: str = LIB_PATH):
 
 
 def _ptr(t):
-    if t is None:
-        return None
-    return ctypes.c_void_p(t.data_ptr())
+    # a plain int (or None): ctypes converts it for the c_void_p argument
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 class _Args:
@@ -163,12 +162,12 @@ class _Args:
             self._fail(name, f"must be a torch.Tensor, got {type(t).__name__}")
         if dtype is not None and t.dtype != dtype:
             self._fail(name, f"must have dtype {dtype}, got {t.dtype}")
-        if shape is not None and tuple(t.shape) != tuple(shape):
+        if shape is not None and t.shape != shape:  # torch.Size compares equal to a tuple
             self._fail(name, f"must have shape {tuple(shape)}, got {tuple(t.shape)}")
         if not t.is_contiguous():
             self._fail(name, "must be contiguous")
-        if min_bytes is not None and t.numel() * t.element_size() < min_bytes:
-            self._fail(name, f"must hold at least {min_bytes} bytes, got {t.numel() * t.element_size()}")
+        if min_bytes is not None and t.nbytes < min_bytes:
+            self._fail(name, f"must hold at least {min_bytes} bytes, got {t.nbytes}")
         self.placed.append((name, t, host))
 
     def absent(self, name, t, why):
@@ -176,18 +175,18 @@ class _Args:
             self._fail(name, f"must be None ({why})")
 
     def done(self):
-        device = None
+        index = None
         for name, t, host in self.placed:
             if host:
-                if t.device.type != "cpu":
+                if not t.is_cpu:
                     self._fail(name, f"must be a host (CPU) tensor, got {t.device}")
                 continue
-            if t.device.type != "cuda":
+            if not t.is_cuda:
                 self._fail(name, f"must be a CUDA tensor, got {t.device}")
-            if device is None:
-                device = t.device
-            elif t.device != device:
-                self._fail(name, f"is on {t.device}, other arguments on {device}")
+            if index is None:
+                index, first = t.get_device(), t
+            elif t.get_device() != index:
+                self._fail(name, f"is on {t.device}, other arguments on {first.device}")
 
 
 def _rows_shape(plan, t, tail):
@@ -271,7 +270,7 @@ def fd_decode_paged(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, block_t
                   workspace, status).done()
     rc = load().fd_decode_paged(ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                 _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse),
-                                _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                _ptr(workspace), workspace.nbytes,
                                 _ptr(status), _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged")
@@ -290,7 +289,7 @@ def fd_decode_paged_ex(plan: FdPlan, q, k_pages, v_pages, k_scale, v_scale, bloc
                         None if cache_leftpad is None else cache_leftpad.data_ptr(), int(cache_rows))
     rc = load().fd_decode_paged_ex(ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                    _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), ctypes.byref(ex), _ptr(out),
-                                   _ptr(lse), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                   _ptr(lse), _ptr(workspace), workspace.nbytes,
                                    _ptr(status), _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged_ex")
@@ -411,7 +410,7 @@ def fd_decode_paged_host(plan: FdPlan, host_in, dev_in, k_pages, v_pages, k_scal
     a.done()
     rc = load().fd_decode_paged_host(ctypes.byref(plan), _ptr(host_in), _ptr(dev_in), _ptr(k_pages), _ptr(v_pages),
                                      _ptr(k_scale), _ptr(v_scale), _ptr(dev_out), _ptr(host_out), _ptr(workspace),
-                                     int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                     workspace.nbytes, _ptr(status),
                                      _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged_host")
@@ -439,7 +438,7 @@ def fd_decode_paged_staged(plan: FdPlan, dev_in, k_pages, v_pages, k_scale, v_sc
     a.done()
     rc = load().fd_decode_paged_staged(ctypes.byref(plan), _ptr(dev_in), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                        _ptr(v_scale), _ptr(dev_out), _ptr(host_out), _ptr(workspace),
-                                       int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                       workspace.nbytes, _ptr(status),
                                        _stream(stream))
     if rc != FD_OK:
         raise FdError(rc, "fd_decode_paged_staged")

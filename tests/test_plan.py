@@ -123,6 +123,21 @@ def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
         assert plan.stages == want_stages
 
 
+@pytest.mark.parametrize("Hq,ps,want_tile,want_stages", [
+    (128, 128, 256, 2),   # G = 16 (two 8-head tiles): two 256-token stages
+    (96, 32, 256, 2),     # G = 12
+    (128, 16, 128, 5),    # 16-token pages: 256-token stages need too many boxes
+    (64, 128, 256, 3),    # G = 8: three
+])
+def test_fp8_two_head_tiles_take_two_256_token_stages(Hq, ps, want_tile, want_stages):
+    prob = _lib.make_problem(64, Hq, 8, 128, ps, 4096 // ps, 64 * (4096 // ps), torch.bfloat16,
+                             torch.float8_e4m3fn)
+    plan = _lib.fd_plan(prob, [4000] * 64, num_sms=152)
+    assert (plan.tile_tokens, plan.stages, plan.ctas_per_sm) == (want_tile, want_stages, 1)
+    # an explicit request keeps 128-token stages
+    assert _lib.fd_plan(prob, [4000] * 64, num_sms=152, tile_tokens=128).tile_tokens == 128
+
+
 SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per CTA
 
 
