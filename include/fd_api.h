@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define FD_API_VERSION 4
+#define FD_API_VERSION 5
 
 typedef enum {
     FD_OK = 0,
@@ -160,7 +160,10 @@ typedef struct {
     int debug_stall_role;
     int q_len;            /* query tokens per sequence (1 = decode); problem.B
                              then counts query rows, B * q_len               */
-    int reserved[3];
+    int scratch_in_stage; /* 1: the item epilogue's scratch lives in the item's
+                             last pipeline stage (16-bit K/V, where that makes
+                             room for another stage); 0: a region of its own */
+    int reserved[2];
 } fd_plan_t;
 
 /* Plan a decode call [P1 §2.1 step 1; P2 进阶突破; P3 §6.3, §8.2].

@@ -67,7 +67,8 @@ class FdPlan(ctypes.Structure):
                 ("ws_counters", ctypes.c_size_t), ("work_items_hint", ctypes.c_longlong),
                 ("kv_rows", ctypes.c_int), ("row_fold", ctypes.c_int), ("head_subgroups", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("timeout_us", ctypes.c_int), ("debug_stall_us", ctypes.c_int),
-                ("debug_stall_role", ctypes.c_int), ("q_len", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("debug_stall_role", ctypes.c_int), ("q_len", ctypes.c_int), ("scratch_in_stage", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n not in ("problem", "reserved")}

@@ -54,11 +54,11 @@ cudaError_t occupancy_kind(const fd_problem &p, const KernelShape &ks, size_t sm
 }
 
 template <int KV, int D, int NT, bool QBF16>
-size_t decode_smem_d(const KernelShape &ks, int stages, int B) {
-    if (ks.consumer_warps == 4 && ks.subtiles == 1) return decode_smem_for<KV, D, NT, 4, 1, QBF16>(stages, B);
-    if (ks.consumer_warps == 8 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 8, 2, QBF16>(stages, B);
-    if (ks.consumer_warps == 4 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 4, 2, QBF16>(stages, B);
-    return decode_smem_for<KV, D, NT, 8, 1, QBF16>(stages, B);
+size_t decode_smem_d(const KernelShape &ks, int stages, int B, bool in_stage) {
+    if (ks.consumer_warps == 4 && ks.subtiles == 1) return decode_smem_for<KV, D, NT, 4, 1, QBF16>(stages, B, in_stage);
+    if (ks.consumer_warps == 8 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 8, 2, QBF16>(stages, B, in_stage);
+    if (ks.consumer_warps == 4 && ks.subtiles == 2) return decode_smem_for<KV, D, NT, 4, 2, QBF16>(stages, B, in_stage);
+    return decode_smem_for<KV, D, NT, 8, 1, QBF16>(stages, B, in_stage);
 }
 
 template <int KV, bool QBF16>
@@ -77,12 +77,12 @@ cudaError_t launch_decode_kind(const fd_problem &p, const KernelShape &ks, const
 }
 
 template <int KV, bool QBF16>
-size_t decode_smem_kind(const fd_problem &p, const KernelShape &ks, int stages) {
+size_t decode_smem_kind(const fd_problem &p, const KernelShape &ks, int stages, bool in_stage) {
     if (p.D == 128)
-        return ks.nt == 1 ? decode_smem_d<KV, 128, 1, QBF16>(ks, stages, p.B)
-                          : decode_smem_d<KV, 128, 2, QBF16>(ks, stages, p.B);
-    return ks.nt == 1 ? decode_smem_d<KV, 64, 1, QBF16>(ks, stages, p.B)
-                      : decode_smem_d<KV, 64, 2, QBF16>(ks, stages, p.B);
+        return ks.nt == 1 ? decode_smem_d<KV, 128, 1, QBF16>(ks, stages, p.B, in_stage)
+                          : decode_smem_d<KV, 128, 2, QBF16>(ks, stages, p.B, in_stage);
+    return ks.nt == 1 ? decode_smem_d<KV, 64, 1, QBF16>(ks, stages, p.B, in_stage)
+                      : decode_smem_d<KV, 64, 2, QBF16>(ks, stages, p.B, in_stage);
 }
 
 }  // namespace fd

@@ -15,8 +15,8 @@ cudaError_t decode_occupancy_e4m3(const fd_problem &p, const KernelShape &ks, si
     return occupancy_kind<KV_E4M3, false>(p, ks, smem, blocks);
 }
 
-size_t decode_smem_e4m3(const fd_problem &p, const KernelShape &ks, int stages) {
-    return decode_smem_kind<KV_E4M3, false>(p, ks, stages);
+size_t decode_smem_e4m3(const fd_problem &p, const KernelShape &ks, int stages, bool in_stage) {
+    return decode_smem_kind<KV_E4M3, false>(p, ks, stages, in_stage);
 }
 
 }  // namespace fd

@@ -13,8 +13,8 @@ cudaError_t decode_occupancy_f16(const fd_problem &p, const KernelShape &ks, siz
     return occupancy_kind<KV_F16, false>(p, ks, smem, blocks);
 }
 
-size_t decode_smem_f16(const fd_problem &p, const KernelShape &ks, int stages) {
-    return decode_smem_kind<KV_F16, false>(p, ks, stages);
+size_t decode_smem_f16(const fd_problem &p, const KernelShape &ks, int stages, bool in_stage) {
+    return decode_smem_kind<KV_F16, false>(p, ks, stages, in_stage);
 }
 
 }  // namespace fd

@@ -84,7 +84,15 @@ struct DecodeShape {
     // Reused for the merge weights (QROWS x kMaxSplits).
     static constexpr int NSLOT = NC >= 8 ? NC / 2 : NC;
     static constexpr int SCR_O = (NSLOT * QROWS * SS > QROWS * kMaxSplits) ? NSLOT * QROWS * SS : QROWS * kMaxSplits;
-    static constexpr int SCRATCH = SCR_O * 4 + 2 * NC * QROWS * 4 + 2 * QROWS * 4 + 16;
+    // The slots and merge weights take a region of their own, or (16-bit
+    // K/V, where a stage holds them and the plan asks for it) the item's
+    // last stage, which the consumers then release only when the item's
+    // epilogue and merge are over: the shared memory this frees goes to
+    // another stage.  Not for 4 warps with two head tiles, whose two CTAs
+    // per SM would no longer fit the register file.
+    static constexpr bool SCR_STAGE_OK = KV != KV_E4M3 && SCR_O * 4 <= STAGE && !(NC == 4 && NT == 2);
+    static constexpr int SCRATCH_SMALL = 2 * NC * QROWS * 4 + 2 * QROWS * 4 + 16;  // per-row m, l, 1/sum, max; flag
+    static constexpr int SCRATCH = SCR_O * 4 + SCRATCH_SMALL;
     static constexpr int THREADS = (NC + 1) * 32;
     static_assert(D == 64 || D == 128, "D");
     static_assert(SUBROW == 128 || SUBROW == 64, "swizzle span");
@@ -425,13 +433,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NST = p.stages;
     uint8_t *stages = smem;
-    float *scratch = reinterpret_cast<float *>(stages + (size_t)NST * Sh::STAGE);
-    float *scr_m = scratch + Sh::SCR_O;
+    const bool scr_in_stage = Sh::SCR_STAGE_OK && p.scr_in_stage;
+    float *scr_own = reinterpret_cast<float *>(stages + (size_t)NST * Sh::STAGE);
+    float *scr_m = scr_own + (scr_in_stage ? 0 : Sh::SCR_O);
     float *scr_l = scr_m + NC * QROWS;
     float *scr_inv = scr_l + NC * QROWS;   // per head: 1 / combined denominator
     float *scr_lse = scr_inv + QROWS;      // per head: combined max (log2 units)
     int *scr_flag = reinterpret_cast<int *>(scr_lse + QROWS);
-    StageMeta *meta = reinterpret_cast<StageMeta *>(reinterpret_cast<uint8_t *>(scratch) + align_up(Sh::SCRATCH, 128));
+    StageMeta *meta = reinterpret_cast<StageMeta *>(reinterpret_cast<uint8_t *>(scr_own) +
+                                                    align_up(scr_in_stage ? Sh::SCRATCH_SMALL : Sh::SCRATCH, 128));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(meta + NST) + 7) & ~uintptr_t(7));
     uint64_t *empty_bar = full_bar + NST;
     // Dispatch tables of the KV rows: item prefix at 32-row block
@@ -1268,12 +1278,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 }
             }
         }
-        // Release the stage (all reads of it are done).
+        // Release the stage (all reads of it are done); an item's last stage
+        // holding the epilogue scratch is released after the epilogue.
         const int m_kvh = mt.kvh, m_s = mt.s, m_nsplit = mt.nsplit, m_hg = mt.hg, m_nrows = mt.nrows;
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+        if (lane == 0 && !(scr_in_stage && (flags & kFlagLast))) mbar_arrive(smem_u32(&empty_bar[st]));
         if (++st == NST) { st = 0; ph ^= 1u; }
         if (!(flags & kFlagLast)) continue;
+        // the stage just consumed: st - 1 (mod NST)
+        float *scratch = scr_in_stage ? reinterpret_cast<float *>(stages + (size_t)((st == 0 ? NST : st) - 1) * Sh::STAGE)
+                                      : scr_own;
+        // every warp's reads of that stage are done before it is written
+        if (scr_in_stage) named_bar_sync(1, NC * 32);
 
         // ========================================================== item epilogue
 #pragma unroll
@@ -1436,16 +1452,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             lrow[n][0] = lrow[n][1] = 0.f;
             qd[n][0] = qd[n][1] = 1.f;
         }
+        // The scratch stage goes back to the producer: this thread's writes
+        // to it are ordered before the copies that refill it.
+        if (scr_in_stage) fence_proxy_async_shared();
         named_bar_sync(1, NC * 32);
+        if (scr_in_stage && lane == 0) mbar_arrive(smem_u32(&empty_bar[(st == 0 ? NST : st) - 1]));
     }
 }
 
+// Dynamic shared memory of this instance with `stages` stages and B KV rows;
+// 0 if the epilogue scratch is asked to live in a stage and cannot.
 template <int KV, int D, int NT, int NC, int SUBT, bool QBF16>
-size_t decode_smem_for(int stages, int B) {
+size_t decode_smem_for(int stages, int B, bool scr_in_stage) {
     using Sh = DecodeShape<KV, D, NT, NC, SUBT>;
+    if (scr_in_stage && !Sh::SCR_STAGE_OK) return 0;
     size_t n = 1024;  // alignment slack
     n += (size_t)stages * Sh::STAGE;
-    n += align_up(Sh::SCRATCH, 128);
+    n += align_up(scr_in_stage ? Sh::SCRATCH_SMALL : Sh::SCRATCH, 128);
     n += (size_t)stages * sizeof(StageMeta);
     n += (size_t)stages * 16;
     n += (size_t)((B + 31) / 32 + 1 + B + kOrderBuckets) * 4 + (size_t)align_up(2 * B, 4);  // dispatch tables

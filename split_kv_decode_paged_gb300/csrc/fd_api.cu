@@ -22,9 +22,9 @@ cudaError_t launch_decode_e4m3(const fd_problem &, const KernelShape &, const De
 cudaError_t decode_occupancy_f16(const fd_problem &, const KernelShape &, size_t, int *);
 cudaError_t decode_occupancy_bf16(const fd_problem &, const KernelShape &, size_t, int *);
 cudaError_t decode_occupancy_e4m3(const fd_problem &, const KernelShape &, size_t, int *);
-size_t decode_smem_f16(const fd_problem &, const KernelShape &, int);
-size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int);
-size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int);
+size_t decode_smem_f16(const fd_problem &, const KernelShape &, int, bool);
+size_t decode_smem_bf16(const fd_problem &, const KernelShape &, int, bool);
+size_t decode_smem_e4m3(const fd_problem &, const KernelShape &, int, bool);
 
 KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold, int ctas_per_sm) {
     KernelShape ks;
@@ -52,11 +52,11 @@ KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold, int cta
     return ks;
 }
 
-size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages) {
+size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages, bool scr_in_stage) {
     switch (p.kv_dtype) {
-    case FD_F16: return decode_smem_f16(p, ks, stages);
-    case FD_BF16: return decode_smem_bf16(p, ks, stages);
-    default: return decode_smem_e4m3(p, ks, stages);
+    case FD_F16: return decode_smem_f16(p, ks, stages, scr_in_stage);
+    case FD_BF16: return decode_smem_bf16(p, ks, stages, scr_in_stage);
+    default: return decode_smem_e4m3(p, ks, stages, scr_in_stage);
     }
 }
 
@@ -383,6 +383,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     struct Shape {
         KernelShape ks;
         int cps = 1, nhg = 1, C = 0, slots = 0, stages = 0;
+        bool scr_in_stage = false;
         size_t smem = 0;
         long long items = 0;
     };
@@ -414,11 +415,29 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         sh.items = 0;
         for (int L : lens) sh.items += (long long)(L == 0 ? 1 : (L + C - 1) / C) * p.Hkv * sh.nhg;
         sh.stages = 0;
+        sh.scr_in_stage = false;
         for (int s = kMaxStages; s >= kMinStages; --s) {
-            const size_t need = decode_smem_bytes(pm, sh.ks, s);
+            const size_t need = decode_smem_bytes(pm, sh.ks, s, false);
             if ((long long)need <= smem_limit(cps)) {
                 sh.stages = s;
                 sh.smem = need;
+                break;
+            }
+        }
+        // 16-bit K/V: the epilogue scratch in the item's last stage, where
+        // that makes room for another stage.  Measured on GB300 (same GPU):
+        // four causal query tokens, two 8-head tiles, 2 -> 3 stages -12%;
+        // GQA groups of 16 -9.5%; one 4096-token sequence of 32 MHA heads on
+        // two CTAs per SM -6.6%; 1024 sequences of 256-1024 tokens -3.7%.  With
+        // the stage count unchanged it only costs (the tiny one-item call
+        // +0.7 us); E4M3 shapes keep their own region (3 instead of 2
+        // 256-token stages with two head tiles measured 9% slower).
+        for (int s = kMaxStages; s > std::max(sh.stages, kMinStages - 1); --s) {
+            const size_t need = decode_smem_bytes(pm, sh.ks, s, true);
+            if (need > 0 && (long long)need <= smem_limit(cps)) {
+                sh.stages = s;
+                sh.smem = need;
+                sh.scr_in_stage = true;
                 break;
             }
         }
@@ -426,11 +445,10 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     };
 
     // Default shape.  E4M3 pools take 256-token stages (8 consumer warps x 2
-    // sub-tiles) when the pages allow them and three stages fit (two stages
-    // with two 8-head tiles, whose per-CTA buffers, ~19 KB larger, leave room
-    // for no third: measured on GB300 with 32 to 128-token pages and G = 12 or 16,
-    // two 256-token stages take 1-7% less time than five 128-token ones);
-    // otherwise 128 (16-bit K/V: always 128).
+    // sub-tiles) when the pages allow them and three stages fit (two suffice
+    // with two 8-head tiles: measured on GB300 with 32 to 128-token pages and
+    // G = 12 or 16, two 256-token stages take 1-7% less time than five
+    // 128-token ones); otherwise 128 (16-bit K/V: always 128).
     const int cps_opt = opt.ctas_per_sm > 0 ? opt.ctas_per_sm : 1;
     int tile_opt = opt.tile_tokens;
     if (q_len > 1) {
@@ -442,7 +460,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     if (tile_opt == 0 && p.kv_dtype == FD_E4M3) {
         const KernelShape k256 = kernel_shape(p, 256, fold, cps_opt);
         const int need = k256.nt == 2 && cps_opt == 1 ? 2 : 3;
-        if (k256.tile == 256 && (long long)decode_smem_bytes(pm, k256, need) <= smem_limit(cps_opt)) tile_opt = 256;
+        if (k256.tile == 256 && (long long)decode_smem_bytes(pm, k256, need, false) <= smem_limit(cps_opt)) tile_opt = 256;
     }
     Shape sh;
     if (!make_shape(tile_opt, cps_opt, sh)) return FD_ERR_UNSUPPORTED;
@@ -540,6 +558,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     plan->num_sms = sms;
     plan->fuse_merge = opt.fuse_merge ? 1 : 0;
     plan->stages = stages;
+    plan->scratch_in_stage = sh.scr_in_stage ? 1 : 0;
     plan->smem_bytes = (int)smem;
     plan->work_items_hint = items;
     plan->kv_rows = kv_rows;
@@ -595,6 +614,14 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
         plan->stages > kMaxStages || plan->grid_ctas < 1 ||
         !hooks_valid(plan->timeout_us, plan->debug_stall_us, plan->debug_stall_role))
         return FD_ERR_INVALID_ARG;
+    // the shared memory the plan grants must hold its layout
+    {
+        fd_problem pk = p;
+        pk.B = plan->kv_rows;
+        if (plan->scratch_in_stage != 0 && plan->scratch_in_stage != 1) return FD_ERR_INVALID_ARG;
+        const size_t need = decode_smem_bytes(pk, ks, plan->stages, plan->scratch_in_stage == 1);
+        if (need == 0 || need > (size_t)std::max(0, plan->smem_bytes)) return FD_ERR_INVALID_ARG;
+    }
 
     const int boxr = std::gcd(p.page_size, ks.tile);
     CUtensorMap tmk, tmv;
@@ -639,6 +666,7 @@ fd_status decode_impl(const fd_plan_t *plan, const void *q, const void *k_pages,
     dp.out_dtype = p.out_dtype;
     dp.fuse_merge = plan->fuse_merge;
     dp.stages = plan->stages;
+    dp.scr_in_stage = plan->scratch_in_stage;
     dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.D));
     dp.timeout_ns = plan->timeout_us > 0 ? (uint64_t)plan->timeout_us * 1000ull : kTimeoutNs;
     dp.stall_ns = (uint64_t)plan->debug_stall_us * 1000ull;

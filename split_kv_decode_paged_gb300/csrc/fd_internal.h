@@ -53,6 +53,7 @@ struct DecodeParams {
     int out_dtype;             // fd_dtype
     int fuse_merge;
     int stages;
+    int scr_in_stage;          // epilogue scratch in the item's last stage (16-bit K/V)
     float scale_log2;          // log2(e) / sqrt(D)
     uint64_t timeout_ns;       // limit of every device-side wait
     uint64_t stall_ns;         // test hook (0 = off): idle time of stall_role
@@ -103,8 +104,10 @@ struct KernelShape {
 // per SM (E4M3 128-token stages with two or more CTAs per SM take 4 consumer
 // warps x 2 sub-tiles, which fit two to an SM).
 KernelShape kernel_shape(const fd_problem &p, int tile_tokens, int fold, int ctas_per_sm);
-size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages);
-int decode_max_stages(const fd_problem &p, const KernelShape &ks);
+// Dynamic shared memory of the decode kernel of this shape with `stages`
+// stages (p.B = KV rows: the dispatch tables); scr_in_stage: the epilogue
+// scratch in the item's last stage (16-bit K/V; 0 where a stage cannot hold it).
+size_t decode_smem_bytes(const fd_problem &p, const KernelShape &ks, int stages, bool scr_in_stage);
 // Resident CTAs per SM of the decode kernel of this shape with smem bytes of
 // dynamic shared memory (needs a device).
 cudaError_t decode_occupancy(const fd_problem &p, const KernelShape &ks, size_t smem, int *blocks);

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(fdlib):
     assert {"fd_plan", "fd_decode_paged", "fd_merge_states", "fd_append_kv", "fd_status_string"} <= declared
     for name in declared:
         assert hasattr(fdlib, name), name
-    assert _lib.fd_api_version() == 4
+    assert _lib.fd_api_version() == 5
 
 
 def _declared_arg_counts():

@@ -107,7 +107,9 @@ def test_head_subgroups_and_shared_kv(fdlib):
     (torch.bfloat16, 128, 256, 256, 128, 3),       # 256-token stages are E4M3 only
     (torch.bfloat16, 16, 1024, 0, 128, 3),
     (torch.bfloat16, 16, 1712, 0, 128, 3),         # the dispatch tables (~6 B per sequence) set
-    (torch.bfloat16, 16, 1728, 0, 128, 2),         # where 3 stages stop fitting ...
+    (torch.bfloat16, 16, 1728, 0, 128, 3),         # where 3 stages stop fitting beside the epilogue
+    (torch.bfloat16, 16, 4475, 0, 128, 3),         # scratch (16-bit K/V: then it moves into a
+    (torch.bfloat16, 16, 4480, 0, 128, 2),         # stage) and where they stop fitting at all ...
     (torch.float8_e4m3fn, 128, 1712, 0, 256, 3),   # ... and where 256-token E4M3 stages do
     (torch.float8_e4m3fn, 128, 1728, 0, 128, None),
     (torch.bfloat16, 16, 8192, 0, 128, 2),         # the largest batch still plans
@@ -121,21 +123,24 @@ def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
     assert plan.smem_bytes <= 232448
     if want_stages is not None:
         assert plan.stages == want_stages
+    # the epilogue scratch moves into a stage only for 16-bit K/V and only
+    # where that buys a stage (1728 <= B <= 4475 here)
+    assert plan.scratch_in_stage == (kv != torch.float8_e4m3fn and 1728 <= B <= 4475)
 
 
-@pytest.mark.parametrize("Hq,ps,want_tile,want_stages", [
-    (128, 128, 256, 2),   # G = 16 (two 8-head tiles): two 256-token stages
-    (96, 32, 256, 2),     # G = 12
-    (128, 16, 128, 5),    # 16-token pages: 256-token stages need too many boxes
-    (64, 128, 256, 3),    # G = 8: three
+@pytest.mark.parametrize("Hq,ps,B,want_tile,want_stages", [
+    (128, 128, 64, 256, 2),    # G = 16 (two 8-head tiles): two 256-token stages
+    (96, 32, 64, 256, 2),      # G = 12
+    (128, 16, 64, 128, 5),     # 16-token pages: 256-token stages need too many boxes
+    (64, 128, 64, 256, 3),     # G = 8: three
 ])
-def test_fp8_two_head_tiles_take_two_256_token_stages(Hq, ps, want_tile, want_stages):
-    prob = _lib.make_problem(64, Hq, 8, 128, ps, 4096 // ps, 64 * (4096 // ps), torch.bfloat16,
+def test_fp8_two_head_tiles_take_two_256_token_stages(Hq, ps, B, want_tile, want_stages):
+    prob = _lib.make_problem(B, Hq, 8, 128, ps, 4096 // ps, B * (4096 // ps), torch.bfloat16,
                              torch.float8_e4m3fn)
-    plan = _lib.fd_plan(prob, [4000] * 64, num_sms=152)
+    plan = _lib.fd_plan(prob, [4000] * B, num_sms=152)
     assert (plan.tile_tokens, plan.stages, plan.ctas_per_sm) == (want_tile, want_stages, 1)
     # an explicit request keeps 128-token stages
-    assert _lib.fd_plan(prob, [4000] * 64, num_sms=152, tile_tokens=128).tile_tokens == 128
+    assert _lib.fd_plan(prob, [4000] * B, num_sms=152, tile_tokens=128).tile_tokens == 128
 
 
 SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per CTA
@@ -146,7 +151,8 @@ SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per 
     (torch.bfloat16, 16, 512, 512, True),
     (torch.bfloat16, 16, 512, 768, True),
     (torch.bfloat16, 16, 512, 1024, False),    # long enough for the default shape
-    (torch.bfloat16, 16, 2048, 1024, True),    # ... unless the default lost a stage to its tables
+    (torch.bfloat16, 16, 2048, 1024, False),   # (three stages, its epilogue scratch in one)
+    (torch.bfloat16, 16, 4480, 1024, True),    # ... unless the default lost a stage to its tables
     (torch.bfloat16, 16, 2048, 2048, False),
     (torch.float8_e4m3fn, 128, 512, 512, True),
     (torch.float8_e4m3fn, 128, 512, 1536, True),
