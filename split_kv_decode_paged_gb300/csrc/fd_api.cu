@@ -100,12 +100,19 @@ constexpr int kDefaultSplitMarginPct = 2;
 // Below this many attended tokens per work item on average (and with enough
 // items), the planner runs two CTAs per SM; for 16-bit K/V the higher figure
 // applies when the default shape has lost pipeline depth to large dispatch
-// tables (measured crossovers on GB300: ~700 and above 1024 tokens).  E4M3
-// K/V switch below 2048 tokens per item when the default shape has 256-token
-// stages, and always otherwise (16-token pages or very large batches, where
-// one producer per SM issuing 2 KB boxes is the limit).
+// tables (measured crossovers on GB300: ~700 and above 1024 tokens).  With
+// TMA boxes of at most 4 KB (16-token pages at D = 128, up to 32-token pages
+// at D = 64) one producer per SM issues them too slowly, and two CTAs (three
+// stages each, their epilogue scratch in a stage) win up to 4096 tokens per
+// item (same GPU, 256-1024 sequences, 8 KV heads: 16-token pages, D = 128,
+// -3.5% at 1024 tokens, -0.7% at 4096; D = 64, 2048 tokens, -24%; 64-token
+// pages, D = 128: +1%, so left to the other figures).  E4M3 K/V switch
+// below 2048 tokens per item when the default shape has 256-token stages,
+// and always otherwise (16-token pages or very large batches, where one
+// producer per SM issuing 2 KB boxes is the limit).
 constexpr double kShortItemTokens = 1024.0;
 constexpr double kShortItemTokensShallow = 1280.0;
+constexpr double kShortItemTokensSmallBox = 4096.0;
 constexpr double kShortItemTokensE4m3 = 2048.0;
 
 // Wait limit (>= 0; 0 = kTimeoutNs) and the stall test hook: off, or a
@@ -476,6 +483,8 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
         double limit;
         if (p.kv_dtype == FD_E4M3)
             limit = sh.ks.tile < 256 ? INFINITY : kShortItemTokensE4m3;
+        else if ((long long)std::gcd(p.page_size, sh.ks.tile) * p.D * 2 <= 4096)
+            limit = kShortItemTokensSmallBox + 1.0;  // up to and including 4096 tokens
         else
             limit = sh.stages < 3 ? kShortItemTokensShallow : kShortItemTokens;
         // E4M3: 128-token stages of 4 warps x 2 sub-tiles; 16-bit: 64-token stages.

@@ -115,9 +115,9 @@ def test_head_subgroups_and_shared_kv(fdlib):
     (torch.bfloat16, 16, 8192, 0, 128, 2),         # the largest batch still plans
 ])
 def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
-    # items of 4000 tokens: long enough that the one-CTA-per-SM shape is kept
-    prob = _lib.make_problem(B, 64, 8, 128, ps, 4096 // ps, B * (4096 // ps), torch.bfloat16, kv)
-    plan = _lib.fd_plan(prob, [4000] * B, num_sms=152, tile_tokens=tile_opt)
+    # items of 8000 tokens: long enough that the one-CTA-per-SM shape is kept
+    prob = _lib.make_problem(B, 64, 8, 128, ps, 8192 // ps, B * (8192 // ps), torch.bfloat16, kv)
+    plan = _lib.fd_plan(prob, [8000] * B, num_sms=152, tile_tokens=tile_opt)
     assert plan.tile_tokens == want_tile
     assert plan.chunk_tokens % plan.tile_tokens == 0
     assert plan.smem_bytes <= 232448
@@ -148,12 +148,14 @@ SM_SMEM, RESERVED = 233472, 1024  # GB300 shared memory per SM and reserved per 
 
 @pytest.mark.parametrize("kv,ps,B,L,want_two", [
     (torch.bfloat16, 16, 512, 256, True),      # short items: two CTAs per SM, 64-token stages
-    (torch.bfloat16, 16, 512, 512, True),
-    (torch.bfloat16, 16, 512, 768, True),
-    (torch.bfloat16, 16, 512, 1024, False),    # long enough for the default shape
-    (torch.bfloat16, 16, 2048, 1024, False),   # (three stages, its epilogue scratch in one)
-    (torch.bfloat16, 16, 4480, 1024, True),    # ... unless the default lost a stage to its tables
-    (torch.bfloat16, 16, 2048, 2048, False),
+    (torch.bfloat16, 16, 512, 1024, True),     # 4 KB boxes (16-token pages, D = 128): items
+    (torch.bfloat16, 16, 2048, 2048, True),    # of up to 4096 tokens
+    (torch.bfloat16, 16, 512, 4096, True),
+    (torch.bfloat16, 64, 512, 512, True),      # 16 KB boxes: below 1024 tokens
+    (torch.bfloat16, 64, 512, 768, True),
+    (torch.bfloat16, 64, 512, 1024, False),    # long enough for the default shape
+    (torch.bfloat16, 64, 4480, 1024, True),    # ... unless the default lost a stage to its tables
+    (torch.bfloat16, 64, 4480, 2048, False),
     (torch.float8_e4m3fn, 128, 512, 512, True),
     (torch.float8_e4m3fn, 128, 512, 1536, True),
     (torch.float8_e4m3fn, 128, 512, 3072, False),  # 256-token stages win on long items
