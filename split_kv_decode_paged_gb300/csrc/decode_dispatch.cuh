@@ -24,8 +24,13 @@ cudaError_t launch_decode_d(const KernelShape &ks, const DecodeParams &dp, const
             return launch_decode_t<KV, D, NT, 8, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);
         if (ks.consumer_warps == 8 && ks.subtiles == 2)
             return launch_decode_t<KV, D, NT, 8, 2, QBF16>(dp, tmk, tmv, grid, smem, stream);
-        if (ks.consumer_warps == 4 && ks.subtiles == 2)
+        if (ks.consumer_warps == 4 && ks.subtiles == 2) {
+            if constexpr (NT == 1) {
+                if (dp.scr_in_stage)
+                    return launch_decode_t<KV, D, NT, 4, 2, QBF16, false, true>(dp, tmk, tmv, grid, smem, stream);
+            }
             return launch_decode_t<KV, D, NT, 4, 2, QBF16>(dp, tmk, tmv, grid, smem, stream);
+        }
     } else {
         if (ks.consumer_warps == 8 && ks.subtiles == 1)
             return launch_decode_t<KV, D, NT, 8, 1, QBF16>(dp, tmk, tmv, grid, smem, stream);

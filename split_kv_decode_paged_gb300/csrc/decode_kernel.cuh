@@ -89,8 +89,11 @@ struct DecodeShape {
     // last stage, which the consumers then release only when the item's
     // epilogue and merge are over: the shared memory this frees goes to
     // another stage.  Not for 4 warps with two head tiles, whose two CTAs
-    // per SM would no longer fit the register file.
-    static constexpr bool SCR_STAGE_OK = KV != KV_E4M3 && SCR_O * 4 <= STAGE && !(NC == 4 && NT == 2);
+    // per SM would no longer fit the register file.  E4M3: only the two-CTA
+    // shape of 4 warps x 2 sub-tiles with one head tile, in an instance of
+    // its own (the other E4M3 instances keep their registers).
+    static constexpr bool SCR_STAGE_OK =
+        (KV != KV_E4M3 || (NC == 4 && SUBT == 2 && NT == 1)) && SCR_O * 4 <= STAGE && !(NC == 4 && NT == 2);
     static constexpr int SCRATCH_SMALL = 2 * NC * QROWS * 4 + 2 * QROWS * 4 + 16;  // per-row m, l, 1/sum, max; flag
     static constexpr int SCRATCH = SCR_O * 4 + SCRATCH_SMALL;
     static constexpr int THREADS = (NC + 1) * 32;
@@ -420,7 +423,8 @@ __device__ __noinline__ void build_dispatch_tables_coop(const DecodeParams &p, i
 // CAUSAL: several query tokens per KV row (DecodeParams::qn > 1), each with
 // its own causal limit; a separate instance so the one-token decode carries
 // none of it.
-template <int KV, int D, int NT, int NC, int SUBT, bool QBF16, bool CAUSAL>
+// SCR: the E4M3 instance that may keep its epilogue scratch in the held stage.
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16, bool CAUSAL, bool SCR = false>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     fd_split_kv_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmv) {
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int NST = p.stages;
     uint8_t *stages = smem;
-    const bool scr_in_stage = Sh::SCR_STAGE_OK && p.scr_in_stage;
+    const bool scr_in_stage = Sh::SCR_STAGE_OK && (KV != KV_E4M3 || SCR) && p.scr_in_stage;
     float *scr_own = reinterpret_cast<float *>(stages + (size_t)NST * Sh::STAGE);
     float *scr_m = scr_own + (scr_in_stage ? 0 : Sh::SCR_O);
     float *scr_l = scr_m + NC * QROWS;
@@ -1485,10 +1489,10 @@ cudaError_t occupancy_t(size_t smem, int *blocks) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, kern, DecodeShape<KV, D, NT, NC, SUBT>::THREADS, smem);
 }
 
-template <int KV, int D, int NT, int NC, int SUBT, bool QBF16, bool CAUSAL = false>
+template <int KV, int D, int NT, int NC, int SUBT, bool QBF16, bool CAUSAL = false, bool SCR = false>
 cudaError_t launch_decode_t(const DecodeParams &dp, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                             size_t smem, cudaStream_t stream) {
-    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16, CAUSAL>;
+    auto kern = fd_split_kv_decode_kernel<KV, D, NT, NC, SUBT, QBF16, CAUSAL, SCR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the kernel may begin its prologue while

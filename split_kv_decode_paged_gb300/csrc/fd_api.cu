@@ -431,15 +431,18 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
                 break;
             }
         }
-        // 16-bit K/V: the epilogue scratch in the item's last stage, where
-        // that makes room for another stage.  Measured on GB300 (same GPU):
-        // four causal query tokens, two 8-head tiles, 2 -> 3 stages -12%;
-        // GQA groups of 16 -9.5%; one 4096-token sequence of 32 MHA heads on
-        // two CTAs per SM -6.6%; 1024 sequences of 256-1024 tokens -3.7%.  With
-        // the stage count unchanged it only costs (the tiny one-item call
-        // +0.7 us); E4M3 shapes keep their own region (3 instead of 2
-        // 256-token stages with two head tiles measured 9% slower).
-        for (int s = kMaxStages; s > std::max(sh.stages, kMinStages - 1); --s) {
+        // The epilogue scratch in the item's last stage, where that makes
+        // room for another stage.  Measured on GB300 (same GPU): four causal
+        // query tokens, two 8-head tiles, 2 -> 3 stages -12%; GQA groups of
+        // 16 -9.5%; one 4096-token sequence of 32 MHA heads on two CTAs per
+        // SM -6.6%; 1024 sequences of 256-1024 tokens -3.7%.  With the stage
+        // count unchanged it only costs (the tiny one-item call +0.7 us).
+        // E4M3: only the two-CTA shape with 2 KB boxes (16-token pages):
+        // 512-768 short sequences -6 to -9%; with 8-16 KB boxes the held
+        // stage delays the next item's first copies (+3 to +8%), and 3
+        // instead of 2 256-token stages with two head tiles measured 9% slower.
+        const bool scr_ok = p.kv_dtype != FD_E4M3 || (long long)std::gcd(p.page_size, sh.ks.tile) * p.D <= 2048;
+        for (int s = kMaxStages; scr_ok && s > std::max(sh.stages, kMinStages - 1); --s) {
             const size_t need = decode_smem_bytes(pm, sh.ks, s, true);
             if (need > 0 && (long long)need <= smem_limit(cps)) {
                 sh.stages = s;

@@ -286,20 +286,23 @@ def test_small_grids_two_ctas_per_sm(fdlib, kv, q, D, H, L, B):
     assert dec.plan.tile_tokens == (128 if kv == "e4m3" else 64)
 
 
-@pytest.mark.parametrize("G,D,ps,splits,fuse,opts", [
-    (16, 128, 16, 0, 1, {}),                 # two head tiles, D = 128: 3 stages instead of 2
-    (16, 128, 64, 12, 1, {}),                # many splits: the merge weights in the held stage
-    (12, 128, 32, 5, 0, {}),                 # ragged head tiles, separate merge
-    (4, 128, 16, 0, 1, {"tile_tokens": 64, "ctas_per_sm": 2}),   # two CTAs per SM: 3 stages
-    (4, 64, 16, 20, 1, {"tile_tokens": 64, "ctas_per_sm": 2}),
+@pytest.mark.parametrize("kv,G,D,ps,splits,fuse,opts", [
+    ("bf16", 16, 128, 16, 0, 1, {}),         # two head tiles, D = 128: 3 stages instead of 2
+    ("bf16", 16, 128, 64, 12, 1, {}),        # many splits: the merge weights in the held stage
+    ("bf16", 12, 128, 32, 5, 0, {}),         # ragged head tiles, separate merge
+    ("bf16", 4, 128, 16, 0, 1, {"tile_tokens": 64, "ctas_per_sm": 2}),   # two CTAs per SM: 3 stages
+    ("bf16", 4, 64, 16, 20, 1, {"tile_tokens": 64, "ctas_per_sm": 2}),
+    ("e4m3", 4, 128, 16, 0, 1, {"tile_tokens": 128, "ctas_per_sm": 2}),  # E4M3, 2 KB boxes
+    ("e4m3", 8, 128, 16, 12, 1, {"tile_tokens": 128, "ctas_per_sm": 2}),
+    ("e4m3", 8, 64, 16, 3, 0, {"tile_tokens": 128, "ctas_per_sm": 2}),
 ])
-def test_epilogue_scratch_in_the_held_stage(fdlib, G, D, ps, splits, fuse, opts):
-    """16-bit K/V plans whose epilogue scratch lives in each item's last
-    stage (held by the consumers until the epilogue and the fused merge are
-    over, so that another stage fits): every row against the oracle, with
-    empty, one-token, page-boundary and ragged lengths, several items per CTA
-    so that held stages are refilled for the next item."""
+def test_epilogue_scratch_in_the_held_stage(fdlib, kv, G, D, ps, splits, fuse, opts):
+    """Plans whose epilogue scratch lives in each item's last stage (held by
+    the consumers until the epilogue and the fused merge are over, so that
+    another stage fits): every row against the oracle, with empty, one-token,
+    page-boundary and ragged lengths, several items per CTA so that held
+    stages are refilled for the next item."""
     lens = [0, 1, 15, 16, 17, 300, 2900, 4100, 64, 999, 129, 2048]
-    spec = _spec(f"held-stage scratch G={G} D={D}", len(lens), 2 * G, 2, D, ps, "bf16", "bf16", lens)
+    spec = _spec(f"held-stage scratch {kv} G={G} D={D}", len(lens), 2 * G, 2, D, ps, kv, "bf16", lens)
     err, dec = _run_and_check(spec, 73 + G + D + splits, num_splits=splits, fuse_merge=fuse, **opts)
     assert dec.plan.scratch_in_stage == 1 and dec.plan.stages >= 3

@@ -123,9 +123,13 @@ def test_stage_shape_selection(kv, ps, B, tile_opt, want_tile, want_stages):
     assert plan.smem_bytes <= 232448
     if want_stages is not None:
         assert plan.stages == want_stages
-    # the epilogue scratch moves into a stage only for 16-bit K/V and only
-    # where that buys a stage (1728 <= B <= 4475 here)
-    assert plan.scratch_in_stage == (kv != torch.float8_e4m3fn and 1728 <= B <= 4475)
+    # the epilogue scratch moves into a stage only where that buys a stage:
+    # 16-bit K/V (1728 <= B <= 4475 here), and E4M3 only on the two-CTA
+    # shape with 2 KB boxes (16-token pages)
+    if kv == torch.float8_e4m3fn:
+        assert plan.scratch_in_stage == (ps == 16 and plan.ctas_per_sm == 2)
+    else:
+        assert plan.scratch_in_stage == (1728 <= B <= 4475)
 
 
 @pytest.mark.parametrize("Hq,ps,B,want_tile,want_stages", [
