@@ -117,11 +117,23 @@ def test_decode_rejects_before_launch(fdlib):
     # scales given for a bf16 cache
     assert L.fd_decode_paged(ctypes.byref(plan), fake, fake, fake, fake, fake, fake, fake, fake, None, fake,
                              plan.workspace_bytes, None, None) == _lib.FD_ERR_INVALID_ARG
+    # a plan whose shared memory does not hold its layout, or whose scratch
+    # placement the shape cannot take
+    for field, value in (("smem_bytes", plan.smem_bytes // 2), ("scratch_in_stage", 2)):
+        bad = _lib.FdPlan.from_buffer_copy(plan)
+        setattr(bad, field, value)
+        assert L.fd_decode_paged(ctypes.byref(bad), fake, fake, fake, None, None, fake, fake, fake, None, fake,
+                                 plan.workspace_bytes, None, None) == _lib.FD_ERR_INVALID_ARG, field
+    p8 = _prob(kv_dtype=torch.float8_e4m3fn)
+    plan8 = _lib.fd_plan(p8, [100, 50], num_sms=148, ctas_per_sm=1)  # one CTA per SM, 8 consumer warps
+    assert plan8.scratch_in_stage == 0
+    plan8.scratch_in_stage = 1  # only the two-CTA E4M3 shape keeps its scratch in a stage
+    assert L.fd_decode_paged(ctypes.byref(plan8), fake, fake, fake, fake, fake, fake, fake, fake, None, fake,
+                             plan8.workspace_bytes, None, None) == _lib.FD_ERR_INVALID_ARG
     # merge: S beyond the maximum
     assert L.fd_merge_states(fake, fake, fake, 1, 1, 5000, 128, _lib.FD_F32, fake, None,
                              None) == _lib.FD_ERR_UNSUPPORTED
     # append: fp8 cache without scales
-    p8 = _prob(kv_dtype=torch.float8_e4m3fn)
     assert L.fd_append_kv(ctypes.byref(p8), fake, fake, fake, fake, None, None, fake, fake, None,
                           None) == _lib.FD_ERR_INVALID_ARG
 
