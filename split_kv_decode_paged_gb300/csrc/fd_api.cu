@@ -523,8 +523,24 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
     // sequence of 32 MHA heads, 16-token pages, 2048 / 4096 tokens -9.6% /
     // -19%; 128-token pages, 4096 tokens -10%; two sequences of 16 heads,
     // 64-token pages, 8192 tokens -3%.
+    // One sequence whose default plan leaves the busiest CTA two or more
+    // items while at most 80% of the slots of its waves hold one (its equal
+    // items cannot balance: e.g. 320 items on 152 SMs, 3 rounds for an average
+    // of 2.1) is planned the same way, when its boxes are at most 2 KB or,
+    // for 16-bit K/V, the two-CTA items keep at least 768 tokens.  Same GPU:
+    // 32 MHA heads over 8192 f16 tokens, 16/32/64/128-token pages, 10 splits
+    // on one CTA per SM 29.3-30.1 us, 9 splits (910 tokens) on two 26.5-26.8
+    // us; E4M3 with 2 KB boxes (16 heads, 16-token pages at D = 128, 32-token
+    // pages at D = 64) -6.3% / -2.4%; left alone: 16 f16 heads over 8192
+    // tokens (19 splits of 431 on two CTAs, +1.8% to -6.4% by page size and
+    // D) and E4M3 with 8-16 KB boxes (16 heads, 16384 tokens, +0.3 / +1.4%).
+    bool medium = false;
+    if (kv_rows == 1 && sh.items >= sms) {
+        const long long waves = (sh.items + sms - 1) / sms;
+        medium = waves >= 2 && (double)sh.items <= 0.8 * (double)(waves * sms);
+    }
     if (q_len == 1 && opt.tile_tokens == 0 && opt.ctas_per_sm == 0 && opt.num_splits == 0 && sh.cps == 1 &&
-        sh.items < sms && maxL > 2 * kMinChunkTokens) {
+        (sh.items < sms || medium) && maxL > 2 * kMinChunkTokens) {
         const int tile2 = p.kv_dtype == FD_E4M3 ? 128 : 64;
         int best_S = 0;
         for (int S = std::min(kMaxSplits, 2 * sms); S >= 1 && best_S == 0; --S) {
@@ -533,7 +549,7 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
                 best_S = S;
         }
         Shape s2;
-        if (best_S > 0 && make_shape(tile2, 2, s2, best_S) && s2.items > sh.items) {
+        if (best_S > 0 && make_shape(tile2, 2, s2, best_S) && (s2.items > sh.items || (medium && s2.items >= sms))) {
             long long tok = 0;
             for (int L : lens) tok += L;
             const double mean_item = (double)tok * p.Hkv * s2.nhg / (double)s2.items;
@@ -545,7 +561,9 @@ fd_status fd_plan(const fd_problem *problem, const int32_t *seq_lens_host, const
                 fits = decode_occupancy(p, s2.ks, s2.smem, &blocks) == cudaSuccess && blocks >= 2;
                 cudaGetLastError();
             }
-            if (fits && (mean_item <= kSmallGridItemTokens || box_bytes <= 2048)) sh = s2;
+            const bool medium_ok =
+                !medium || box_bytes <= 2048 || (p.kv_dtype != FD_E4M3 && mean_item >= 768.0);
+            if (fits && medium_ok && (mean_item <= kSmallGridItemTokens || box_bytes <= 2048)) sh = s2;
         }
     }
     const KernelShape ks = sh.ks;

@@ -274,7 +274,8 @@ def test_fp8_two_ctas_128_token_stages(fdlib, Hq, D, splits, fuse):
                                           ("f16", "f16", 128, 32, 2048, 1),
                                           ("bf16", "bf16", 128, 16, 4096, 2),
                                           ("f16", "f16", 128, 32, 3000, 1),
-                                          ("e4m3", "bf16", 128, 32, 3000, 1)])
+                                          ("e4m3", "bf16", 128, 32, 3000, 1),
+                                          ("f16", "f16", 128, 32, 8192, 1)])  # an imbalanced one-CTA plan
 def test_small_grids_two_ctas_per_sm(fdlib, kv, q, D, H, L, B):
     """Fewer items than SMs: the planner's small-grid shape (two CTAs per SM,
     64-token stages, more splits, fused merge) against the oracle on every

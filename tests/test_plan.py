@@ -191,6 +191,9 @@ def test_short_items_take_two_ctas_per_sm(kv, ps, B, L, want_two):
     (1, 4, 64, 256, torch.float16, False, 1),        # short sequence: not split
     (1, 32, 128, 1024, torch.float16, False, 4),     # at most 2 x 256 tokens would remain per item
     (1, 32, 128, 4096, torch.float8_e4m3fn, True, 8),  # E4M3: 128-token stages of 4 warps x 2
+    (1, 32, 128, 8192, torch.float16, True, 9),      # 320 items on one CTA per SM cannot balance
+    (1, 16, 128, 8192, torch.float16, False, 10),    # ... left alone with 431-token items, 4 KB boxes
+    (1, 16, 128, 8192, torch.float8_e4m3fn, True, 16),  # ... taken with 2 KB boxes
 ])
 def test_small_grids_take_two_ctas_per_sm(fdlib, B, H, D, L, kv, want_two, want_splits):
     """Fewer work items than SMs: two CTAs per SM with the most splits whose
